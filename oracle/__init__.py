@@ -1,0 +1,159 @@
+"""fp64 CPU oracle for the PillarAttn unified step -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It restates, in plain C compiled with
+gcc, what the GPU path computes (see ``pillar_oracle.c`` for the page
+citations and the readings of points the pages leave open).  It shares no
+code with the CUDA library and never calls it.
+
+Pins: every function here is checked by ``tests/test_oracle_pins.py``
+against closed forms, invariants and brute force.  Nothing in it is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pillar_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "libpillar_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain C11, -O2, no target-specific flags)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".{os.getpid()}.tmp"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i32, i64, f64 = ctypes.c_int, ctypes.c_longlong, ctypes.c_double
+        lib.oracle_attn_unified.argtypes = [i32, i32, i32, i32, i32, i64, f64, i32,
+                                            P, P, P, P, P, P, P, P, P, P, P, P, i32]
+        lib.oracle_attn_unified.restype = i32
+        lib.oracle_topk_select.argtypes = [i32, i32, i32, i32, i32, i32, i32,
+                                           P, P, P, P, P, P, P, i32]
+        lib.oracle_topk_select.restype = i32
+        lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_f64.restype = f64
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def bf16_to_f64(bits: int) -> float:
+    """Exact value of one bf16 bit pattern (the oracle's own widening)."""
+    return float(_load().oracle_bf16_to_f64(int(bits) & 0xFFFF))
+
+
+@dataclass
+class AttnResult:
+    out: np.ndarray        # [T_q, Hq, D] fp64
+    lse: np.ndarray        # [T_q, Hq] fp64 (draft rows included)
+    logits: np.ndarray     # packed [sum_v Hq*(k+1)*L_v] fp64 (selected verify requests)
+    status: int
+
+
+def attn_unified(*, Hq, Hkv, D, k, scale, q, k_pool, v_pool, slot_table, req_mode, req_len,
+                 sparse_idx, sparse_cnt, select=None, want_logits=True, nthreads=None):
+    """Run the unified draft/verify step in fp64 (see ``oracle_attn_unified``).
+
+    bf16 arrays are passed as their uint16 bit patterns.  ``select`` (bool [B])
+    restricts the work to some requests; the logits buffer is then packed over
+    the selected verify requests only.
+    """
+    req_mode = _c(req_mode, np.int32)
+    req_len = _c(req_len, np.int32)
+    B = int(req_mode.shape[0])
+    q = _c(q, np.uint16)
+    T_q = int(q.shape[0])
+    sparse_idx = _c(sparse_idx, np.int32)
+    max_sparse = int(sparse_idx.shape[-1]) if sparse_idx.size else 0
+    sel = None if select is None else _c(np.asarray(select).astype(bool), np.uint8)
+    out = np.zeros((T_q, Hq, D), np.float64)
+    lse = np.full((T_q, Hq), np.nan, np.float64)
+    ver = (req_mode == 1) if sel is None else ((req_mode == 1) & sel.astype(bool))
+    n_logits = int(Hq * (k + 1) * req_len[ver].astype(np.int64).sum()) if want_logits else 0
+    logits = np.empty(n_logits, np.float64) if want_logits else None
+    st = _load().oracle_attn_unified(
+        B, Hq, Hkv, D, k, int(k_pool.shape[0]), float(scale), max_sparse,
+        _ptr(q), _ptr(_c(k_pool, np.uint16)), _ptr(_c(v_pool, np.uint16)),
+        _ptr(_c(slot_table, np.int32)), _ptr(req_mode), _ptr(req_len),
+        _ptr(sparse_idx), _ptr(_c(sparse_cnt, np.int32)), _ptr(sel),
+        _ptr(out), _ptr(lse), _ptr(logits), int(nthreads or default_threads()))
+    if st == -1:
+        raise ValueError("oracle_attn_unified: bad dimensions")
+    if st == -5:
+        raise MemoryError("oracle_attn_unified")
+    return AttnResult(out, lse, logits if logits is not None else np.empty(0), st)
+
+
+@dataclass
+class TopkResult:
+    next_idx: np.ndarray   # [V, Hkv, max_topk] int32 (first next_cnt entries valid)
+    next_cnt: np.ndarray   # [V, Hkv] int32
+    scores: np.ndarray     # packed [sum_v Hkv*L_v] fp64
+    status: int
+
+
+def topk_select(*, Hq, Hkv, k, row_lo, row_hi, logits, lse, L, K, max_topk, nthreads=None):
+    """Averaged exact scores and Top-K per (verify request, KV head), in fp64.
+
+    ``logits`` is packed [V][Hq][k+1][L_v]; ``lse`` is [V, Hq, k+1].
+    """
+    L = _c(L, np.int32)
+    K = _c(K, np.int32)
+    V = int(L.shape[0])
+    logits = _c(logits, np.float64)
+    lse = _c(lse, np.float64)
+    next_idx = np.full((V, Hkv, max(max_topk, 1)), -1, np.int32)
+    next_cnt = np.zeros((V, Hkv), np.int32)
+    scores = np.empty(int(Hkv * L.astype(np.int64).sum()), np.float64)
+    st = _load().oracle_topk_select(V, Hq, Hkv, k, row_lo, row_hi, max_topk, _ptr(logits), _ptr(lse),
+                                    _ptr(L), _ptr(K), _ptr(next_idx), _ptr(next_cnt), _ptr(scores),
+                                    int(nthreads or default_threads()))
+    if st == -5:
+        raise MemoryError("oracle_topk_select")
+    if st == -1 and V:
+        raise ValueError("oracle_topk_select: bad arguments")
+    return TopkResult(next_idx[:, :, :max_topk], next_cnt, scores, st)
+
+
+def verify_lse_of(res: AttnResult, req_mode, k, Hq, select=None):
+    """Gather the verify rows' LSE into the [V, Hq, k+1] layout of the GPU dump."""
+    req_mode = np.asarray(req_mode)
+    rows = []
+    q_off = 0
+    for b, m in enumerate(req_mode):
+        n = k + 1 if m == 1 else 1
+        if m == 1 and (select is None or select[b]):
+            rows.append(res.lse[q_off:q_off + n, :].T)  # [Hq, k+1]
+        q_off += n
+    if not rows:
+        return np.zeros((0, Hq, k + 1))
+    return np.stack(rows, 0)
