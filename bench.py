@@ -1,0 +1,372 @@
+"""Benchmark of the PillarAttn unified step on GB300.
+
+One step = pillar_attn_unified (planner + persistent unified draft/verify
+kernel, with the logits/LSE dump) + pillar_topk_select (score
+rematerialisation, averaging, Top-K) over one batch of the Qwen3-8B-shaped
+workload: 128 requests (1/9 verify with 9 query rows, 8/9 draft), 32 query
+heads, 8 KV heads, head_dim 128, bf16, contexts uniform in [6144, 10240],
+k = 8, s = 0.05, a randomly permuted page-size-1 KV pool.  Inputs are seeded
+synthetic data of that shape (see workloads/).
+
+Prints one JSON line (rank 0).  value = microseconds per layer-step (lower
+is better); under torchrun every rank runs its own replica of the workload
+(weak scaling) and value = max-over-ranks time / layer-steps of all ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle as the reference arm
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "PillarAttn unified step: µs/layer-step, KV-read GB/s and % of HBM peak"
+UNIT = "us/layer-step"
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["pillar_attn.cu", "pillar_plan.cu", "pillar_device.cuh", "pillar_internal.h"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="qwen3_8b")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "sparse_self_speculative_pillar_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """dram bytes per launch of the unified kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"unified_attn_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("source_sha") != kernel_source_hash():
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv") if os.path.isdir(
+            os.path.join(ROOT, "gpurun_out")) else f"/tmp/pillar_clocks_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- oracle timing (CPU)
+
+def oracle_sample_time(w, nthreads, budget_s=20.0):
+    """Time the fp64 oracle on a bounded sample of the workload (one verify
+    request of median length, the draft requests next to it, and the Top-K of
+    that verify request) and extrapolate to a full step by algorithmic KV bytes."""
+    import oracle
+    ver = np.nonzero(w.req_mode == 1)[0]
+    dra = np.nonzero(w.req_mode == 0)[0]
+    sel = np.zeros(w.B, bool)
+    vb = ver[np.argsort(w.req_len[ver])[len(ver) // 2]] if len(ver) else None
+    if vb is not None:
+        sel[vb] = True
+    sel[dra[:min(len(dra), 16)]] = True
+    row = w.D * 2 * 2
+    def kv_bytes(mask):
+        vm = mask & (w.req_mode == 1)
+        dm = mask & (w.req_mode == 0)
+        return (int(w.req_len[vm].astype(np.int64).sum()) * w.Hkv * row +
+                int(w.sparse_cnt[dm].astype(np.int64).sum()) * row)
+    total = kv_bytes(np.ones(w.B, bool))
+    samp = kv_bytes(sel)
+    t0 = time.perf_counter()
+    r = oracle.attn_unified(Hq=w.Hq, Hkv=w.Hkv, D=w.D, k=w.k, scale=1 / math.sqrt(w.D), q=w.q, k_pool=w.k_logical,
+                            v_pool=w.v_logical, slot_table=np.arange(len(w.slot_table), dtype=np.int32),
+                            req_mode=w.req_mode, req_len=w.req_len, sparse_idx=w.sparse_idx,
+                            sparse_cnt=w.sparse_cnt, select=sel, nthreads=nthreads)
+    t_attn = time.perf_counter() - t0
+    t_topk = 0.0
+    if vb is not None:
+        t0 = time.perf_counter()
+        vi = list(ver).index(vb)
+        oracle.topk_select(Hq=w.Hq, Hkv=w.Hkv, k=w.k, row_lo=1, row_hi=w.k + 1, logits=r.logits,
+                           lse=oracle.verify_lse_of(r, w.req_mode, w.k, w.Hq, select=sel),
+                           L=w.verify_len[vi:vi + 1], K=w.topk_K[vi:vi + 1], max_topk=int(w.topk_K[vi]),
+                           nthreads=nthreads)
+        t_topk = (time.perf_counter() - t0) * len(ver)   # Top-K cost scales with the verify count
+    scale = total / max(1, samp)
+    est_us = (t_attn * scale + t_topk) * 1e6
+    desc = (f"fp64 oracle on 1 verify request (L={int(w.req_len[vb]) if vb is not None else 0}) + "
+            f"{int(sel.sum()) - (vb is not None)} draft requests of the {w.recipe.name} batch "
+            f"({samp / 1e6:.1f} of {total / 1e6:.1f} MB algorithmic KV) took {t_attn:.2f} s, "
+            f"plus Top-K of that verify request; scaled to the full layer-step by KV bytes")
+    return est_us, desc, t_attn
+
+
+# --------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = W.generate(args.workload)
+    nthreads = os.cpu_count() or 1
+    budget = 150.0
+    t_start = time.perf_counter()
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        if time.perf_counter() - t_start > budget and len(per_step) >= 1:
+            break
+        est_us, desc, _ = oracle_sample_time(w, nthreads)
+        if i >= args.warmup or args.steps == 0:
+            per_step.append(est_us)
+        if time.perf_counter() - t_start > budget and per_step:
+            break
+    value = statistics.median(per_step) if per_step else None
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3 if value else None,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.recipe.name, "global_batch": int(w.B), "seq_len": int(w.req_len.mean()),
+                   "parallelism": "replicas" if args.gpus > 1 else "single"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+                         "sample": desc + f"; median over {len(per_step)} timed samples"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    import sparse_self_speculative_pillar_gb300 as P
+    from tests._gpu_common import Gpu
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    P.load()
+
+    # each rank: its own replica of the workload (distinct seed)
+    rec = W.RECIPES[args.workload]
+    if rank:
+        rec = W.scaled(args.workload, seed_offset=1000 * rank)
+    w = W.generate(rec)
+    g = Gpu(w)
+    ab = W.algorithmic_bytes(w)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        g.attn(stream)
+        g.topk(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    flags = g.attn_flags() | g.topk_flags()
+    if flags:
+        raise RuntimeError(f"device error flags 0x{flags:x} during warm-up")
+
+    # per-call events over the timed region (on the launching stream)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        g.attn(stream)
+        ev[i][1].record(stream)
+        g.topk(stream)
+        ev[i][2].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    attn_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    topk_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    us_per_step = elapsed_ms * 1e3 / (args.steps * world)
+
+    # end to end: per-step inputs from pinned host memory, results back to host
+    e2e_steps = args.e2e_steps or max(10, min(args.steps, 500))
+    h_in = {n: getattr(g, n).cpu().pin_memory() for n in
+            ("q", "slot_table", "req_mode", "req_len", "sparse_idx", "sparse_cnt", "group_map", "K")}
+    h_out = {n: torch.empty_like(getattr(g, n), device="cpu").pin_memory() for n in ("out", "next_idx", "next_cnt")}
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for n, t in h_in.items():
+            getattr(g, n).copy_(t, non_blocking=True)
+        step()
+        for n, t in h_out.items():
+            t.copy_(getattr(g, n), non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_us = e2e_ms * 1e3 / (e2e_steps * world)
+    flags = g.attn_flags() | g.topk_flags()
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peak, peak_kind = measured_peak()
+    attn_s = attn_ms / 1e3
+    achieved = ab["attn_total"] / attn_s / 1e9
+    kv_gbs = ab["kv"] / attn_s / 1e9
+    step_gbs = ab["step_total"] / (us_per_step * world / 1e6) / 1e9 if world == 1 else None
+    traffic = profiled_traffic(w.recipe.name)
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        est_us, desc, _ = oracle_sample_time(w, os.cpu_count() or 1)
+        cpu = {"value": est_us, "unit": UNIT, "cores": os.cpu_count() or 1, "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC, "value": us_per_step, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us_per_step / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.recipe.name, "global_batch": int(w.B) * world, "seq_len": int(w.req_len.mean()),
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "verify_requests": int(w.V), "draft_requests": int(w.B - w.V),
+                   "heads": f"{w.Hq}q/{w.Hkv}kv", "head_dim": int(w.D), "k": int(w.k),
+                   "l2": "inputs larger than L2 (KV read per step %.0f MB)" % (ab["kv"] / 1e6)},
+        "attn_us": attn_ms * 1e3, "topk_us": topk_ms * 1e3,
+        "kv_read_gbs": kv_gbs, "kv_read_frac_of_peak": kv_gbs / peak,
+        "kv_read_frac_of_nominal": kv_gbs / NOMINAL_HBM_GBS,
+        "step_algorithmic_gbs": step_gbs,
+        "algorithmic_bytes": ab,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "pillar_attn_unified (planner + unified kernel), event-timed per call",
+                     "peak_kind": peak_kind},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+        "device_flags": flags,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,175 @@
+/*
+ * pillar.h -- C ABI of the GB300 (sm_103a) PillarAttn unified step.
+ *
+ * The method ("SparseSpec-MLSys26", section 核心方法 / PillarAttn):
+ *   - a draft request (one query token) attends only its critical-token list,
+ *     one list per (request, KV head);
+ *   - a verify request (k+1 query tokens, causal among themselves) attends
+ *     its full context and, in the same pass, dumps the raw attention logits
+ *     and the log-sum-exp of every row;
+ *   - from that dump the exact softmax scores are rematerialised, averaged
+ *     over the k draft rows and the GQA group's query heads, and the Top-K
+ *     positions (K = ceil(s*len)) become the next stride's critical list.
+ * With a page-size-1 KV pool every position reaches its K/V row through a
+ * per-request slot table, so sparse and full attention share one pipeline
+ * and mix freely in one batch (same page, section "Unified batch scheduler
+ * + fused attention kernel").
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers owned by the caller.  The
+ *     library allocates nothing and keeps no state between calls, except the
+ *     per-device launch attributes it sets once.  Scratch lives in the
+ *     caller's workspace (sized by the *_workspace_bytes functions); the
+ *     device error word sits inside that workspace.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on that stream: a return of PILLAR_OK means the work was
+ *     validated and enqueued.  Data-dependent problems found on the device
+ *     (an index or slot out of range, a bad mode or length) are skipped and
+ *     recorded in the error word; read it with pillar_get_error.
+ *   - Nothing on the device waits without a bound: a wait that runs past
+ *     about one second records PILLAR_FLAG_TIMEOUT and the kernel returns.
+ */
+#ifndef PILLAR_H
+#define PILLAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PILLAR_API __attribute__((visibility("default")))
+#else
+#define PILLAR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define PILLAR_OK 0
+#define PILLAR_ERR_ARG (-1)         /* null pointer, bad dimension or unsupported shape */
+#define PILLAR_ERR_WORKSPACE (-2)   /* workspace null, misaligned or too small */
+#define PILLAR_ERR_CUDA (-3)        /* a CUDA runtime call or launch failed */
+#define PILLAR_ERR_DEVICE (-4)      /* pillar_get_error: the device error word is non-zero */
+
+/* Bits of the device error word. */
+#define PILLAR_FLAG_INDEX 1         /* a critical-list position outside [0, L_b) was skipped */
+#define PILLAR_FLAG_SLOT 2          /* a slot outside [0, num_slots) was skipped */
+#define PILLAR_FLAG_REQUEST 4       /* req_mode not 0/1, L_b < 0, L_b > max_len, or verify L_b < k+1 */
+#define PILLAR_FLAG_COUNT 8         /* sparse_cnt outside [0, max_sparse] (clamped) */
+#define PILLAR_FLAG_TIMEOUT 16      /* a bounded device wait gave up; outputs are incomplete */
+#define PILLAR_FLAG_TOPK 32         /* a Top-K budget exceeded max_topk (clamped) */
+
+typedef struct pillar_shape {
+    int32_t B;             /* requests in the batch (>= 0) */
+    int32_t Hq;            /* query heads */
+    int32_t Hkv;           /* KV heads; G = Hq / Hkv query heads share one (1 <= G <= 8) */
+    int32_t D;             /* head dimension: 64 or 128 */
+    int32_t k;             /* stride: a verify request carries k+1 query rows; (k+1)*G <= 64 */
+    int32_t max_sparse;    /* row stride of sparse_idx (>= 0) */
+    int32_t max_len;       /* upper bound on every req_len; sizes the workspace (>= 1) */
+    int32_t row_lo;        /* verify rows [row_lo, row_hi) are averaged by Top-K; */
+    int32_t row_hi;        /*   the k draft rows are [1, k+1) */
+    int32_t max_topk;      /* row stride of next_idx (>= 1) */
+    int32_t verify_chunk;  /* keys per verify work item (multiple of 64; 0 = 1024) */
+    int32_t draft_chunk;   /* listed keys per draft work item (multiple of 64; 0 = 2048) */
+    int64_t num_slots;     /* rows of k_pool / v_pool */
+    float sm_scale;        /* logit scale; 0 means 1/sqrt(D) */
+    int32_t reserved;      /* must be 0 */
+} pillar_shape_t;
+
+/*
+ * pillar_attn_workspace_bytes -- bytes of workspace pillar_attn_unified
+ * needs for this shape (a bound over every batch with req_len <= max_len and
+ * sparse_cnt <= max_sparse).  Returns PILLAR_OK or PILLAR_ERR_ARG.
+ */
+PILLAR_API int pillar_attn_workspace_bytes(const pillar_shape_t *shape, size_t *bytes);
+
+/*
+ * pillar_attn_unified -- one unified draft/verify attention step.
+ * ("SparseSpec-MLSys26", 核心方法 / PillarAttn: sparse draft attention over
+ * the critical set, full verify attention with the logits/LSE dump; and the
+ * unified-batch section: page size 1, one fused pass over mixed requests.)
+ *
+ *   q            [T_q, Hq, D] bf16.  Requests packed in batch order: one row
+ *                for a draft request, k+1 rows for a verify request.
+ *   k_pool,
+ *   v_pool       [num_slots, Hkv, D] bf16: one slot = one token, all heads.
+ *   slot_table   int32; request b's L_b slots start at sum_{b'<b} L_b'.
+ *                slot_table[off_b + t] is the slot of position t.
+ *   req_mode     [B] int32: 0 draft, 1 verify.
+ *   req_len      [B] int32: L_b, the context length including the request's
+ *                own new tokens.  Verify row j (0..k) sits at position
+ *                L_b-(k+1)+j and attends positions [0, L_b-(k+1)+j].
+ *   sparse_idx   [B, Hkv, max_sparse] int32 logical positions (draft only);
+ *   sparse_cnt   [B, Hkv] int32 list lengths.  Query head h uses KV head
+ *                h / G and that head's list, taken literally (a repeated
+ *                position counts twice).  An empty list gives a zero output.
+ *   out          [T_q, Hq, D] bf16: attention output of every query row.
+ *   verify_logits  fp32, packed over the verify requests in batch order:
+ *                [V][Hq][k+1][L_v], the scaled logits q.k*scale, -inf where
+ *                the row may not look (t beyond its causal limit).
+ *   verify_lse   [V][Hq][k+1] fp32: natural-log LSE of each verify row.
+ *   workspace    device scratch of at least pillar_attn_workspace_bytes,
+ *                256-byte aligned.  Must not be shared by concurrent calls.
+ *
+ * Returns PILLAR_OK, PILLAR_ERR_ARG, PILLAR_ERR_WORKSPACE or PILLAR_ERR_CUDA.
+ * With B == 0 nothing is launched.
+ */
+PILLAR_API int pillar_attn_unified(const pillar_shape_t *shape, const uint16_t *q, const uint16_t *k_pool,
+                        const uint16_t *v_pool, const int32_t *slot_table, const int32_t *req_mode,
+                        const int32_t *req_len, const int32_t *sparse_idx, const int32_t *sparse_cnt,
+                        uint16_t *out, float *verify_logits, float *verify_lse, void *workspace,
+                        size_t ws_bytes, void *stream);
+
+/*
+ * pillar_topk_workspace_bytes -- workspace of pillar_topk_select for V
+ * verify requests of length <= max_len.
+ */
+PILLAR_API int pillar_topk_workspace_bytes(const pillar_shape_t *shape, int32_t V, size_t *bytes);
+
+/*
+ * pillar_topk_select -- the next stride's critical lists from one verify
+ * pass ("SparseSpec-MLSys26", 核心方法 / PillarAttn: rematerialise exact
+ * scores from the dumped logits and LSE, average over the k draft rows and
+ * the GQA group's heads, take Top-K).
+ *
+ *   V              number of verify requests (host value).
+ *   verify_logits,
+ *   verify_lse     as written by pillar_attn_unified.
+ *   req_len        [B] int32, as given to pillar_attn_unified.
+ *   group_map      [V] int32: batch index b of the v-th verify request, in
+ *                  increasing order (it fixes L_v and the logits offsets).
+ *   K              [V] int32: K_v, the number of positions to keep; clamped
+ *                  to [0, L_v], and to max_topk with PILLAR_FLAG_TOPK.
+ *   next_idx       [V, Hkv, max_topk] int32: the selected positions of KV
+ *                  head g, ascending; entries past next_cnt are untouched.
+ *   next_cnt       [V, Hkv] int32: number of selected positions.
+ * For KV head g and position t in [0, L_v):
+ *   score[t] = 1/((row_hi-row_lo)*G) * sum_{r in [row_lo,row_hi)}
+ *              sum_{h in group g} exp(logit[h][r][t] - lse[h][r])
+ * (masked logits contribute 0).  The K_v largest scores are kept, equal
+ * scores taken lowest position first.  Scores are formed in fp32.
+ */
+PILLAR_API int pillar_topk_select(const pillar_shape_t *shape, int32_t V, const float *verify_logits,
+                       const float *verify_lse, const int32_t *req_len, const int32_t *group_map,
+                       const int32_t *K, int32_t *next_idx, int32_t *next_cnt, void *workspace,
+                       size_t ws_bytes, void *stream);
+
+/*
+ * pillar_get_error -- synchronises `stream`, then copies the device error
+ * word of a workspace (either entry point's) into *flags and clears it.
+ * Returns PILLAR_OK if it was zero, PILLAR_ERR_DEVICE if not,
+ * PILLAR_ERR_ARG / PILLAR_ERR_CUDA on failure.
+ */
+PILLAR_API int pillar_get_error(void *workspace, void *stream, int32_t *flags);
+
+/* pillar_status_string -- a static English description of a return code. */
+PILLAR_API const char *pillar_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PILLAR_H */

@@ -1,0 +1,183 @@
+"""GB300 (sm_103a) PillarAttn unified step: thin Python binding over the C ABI.
+
+Every step of the path runs in the CUDA library built from ``csrc/``; this
+module only marshals arguments (torch tensors or raw device pointers) into
+the ``extern "C"`` entry points declared in ``include/pillar.h`` and turns
+non-zero status codes into exceptions.  There is no fallback: if the
+library is missing or cannot be loaded, every call raises.
+
+Entry points (same names as the C ABI):
+  pillar_attn_workspace_bytes(shape)
+  pillar_attn_unified(shape, q, k_pool, v_pool, slot_table, req_mode, req_len,
+                      sparse_idx, sparse_cnt, out, verify_logits, verify_lse,
+                      workspace, stream=None)
+  pillar_topk_workspace_bytes(shape, V)
+  pillar_topk_select(shape, V, verify_logits, verify_lse, req_len, group_map, K,
+                     next_idx, next_cnt, workspace, stream=None)
+  pillar_get_error(workspace, stream=None)
+  pillar_status_string(status)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+__all__ = [
+    "PillarShape", "make_shape", "PillarError", "load", "library_path", "build",
+    "pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_topk_workspace_bytes",
+    "pillar_topk_select", "pillar_get_error", "pillar_status_string",
+    "FLAG_INDEX", "FLAG_SLOT", "FLAG_REQUEST", "FLAG_COUNT", "FLAG_TIMEOUT", "FLAG_TOPK",
+]
+
+FLAG_INDEX, FLAG_SLOT, FLAG_REQUEST, FLAG_COUNT, FLAG_TIMEOUT, FLAG_TOPK = 1, 2, 4, 8, 16, 32
+EXPORTED = ("pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_topk_workspace_bytes",
+            "pillar_topk_select", "pillar_get_error", "pillar_status_string")
+
+
+class PillarShape(ctypes.Structure):
+    """Mirror of ``pillar_shape_t``."""
+    _fields_ = [
+        ("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("D", ctypes.c_int32),
+        ("k", ctypes.c_int32), ("max_sparse", ctypes.c_int32), ("max_len", ctypes.c_int32),
+        ("row_lo", ctypes.c_int32), ("row_hi", ctypes.c_int32), ("max_topk", ctypes.c_int32),
+        ("verify_chunk", ctypes.c_int32), ("draft_chunk", ctypes.c_int32), ("num_slots", ctypes.c_int64),
+        ("sm_scale", ctypes.c_float), ("reserved", ctypes.c_int32),
+    ]
+
+
+def make_shape(*, B, Hq, Hkv, D, k, max_sparse, max_len, num_slots, max_topk=1, row_lo=1, row_hi=None,
+               verify_chunk=0, draft_chunk=0, sm_scale=0.0) -> PillarShape:
+    return PillarShape(B=B, Hq=Hq, Hkv=Hkv, D=D, k=k, max_sparse=max_sparse, max_len=max_len,
+                       row_lo=row_lo, row_hi=(k + 1) if row_hi is None else row_hi, max_topk=max(1, max_topk),
+                       verify_chunk=verify_chunk, draft_chunk=draft_chunk, num_slots=num_slots,
+                       sm_scale=sm_scale, reserved=0)
+
+
+class PillarError(RuntimeError):
+    def __init__(self, fn, status, flags=None):
+        self.status = status
+        self.flags = flags
+        msg = f"{fn}: status {status} ({pillar_status_string(status)})"
+        if flags is not None:
+            msg += f", device flags 0x{flags:x}"
+        super().__init__(msg)
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def build(force: bool = False) -> str:
+    return _build.build(force=force)
+
+
+def load():
+    """Load the CUDA library (built in-tree by ``build()``); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"the sm_103a library is not built ({path}); run __graft_entry__.build()")
+    import torch  # noqa: F401  -- makes the CUDA runtime of the process available first
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    SP = ctypes.POINTER(PillarShape)
+    lib.pillar_attn_workspace_bytes.argtypes = [SP, ctypes.POINTER(ctypes.c_size_t)]
+    lib.pillar_attn_unified.argtypes = [SP] + [P] * 11 + [P, ctypes.c_size_t, P]
+    lib.pillar_topk_workspace_bytes.argtypes = [SP, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]
+    lib.pillar_topk_select.argtypes = [SP, ctypes.c_int32] + [P] * 7 + [P, ctypes.c_size_t, P]
+    lib.pillar_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
+    lib.pillar_status_string.argtypes = [ctypes.c_int]
+    lib.pillar_status_string.restype = ctypes.c_char_p
+    for n in EXPORTED[:-1]:
+        getattr(lib, n).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    """Device pointer of a CUDA tensor (or a raw int pointer, or None)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if not x.is_cuda:
+        raise ValueError("device tensors only")
+    if not x.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return x.data_ptr()
+
+
+def _nbytes(x):
+    if isinstance(x, int):
+        raise ValueError("a raw workspace pointer needs an explicit size")
+    return x.numel() * x.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def pillar_status_string(status: int) -> str:
+    if _lib is None:
+        try:
+            load()
+        except Exception:  # pragma: no cover
+            return "library not loaded"
+    return _lib.pillar_status_string(int(status)).decode()
+
+
+def pillar_attn_workspace_bytes(shape: PillarShape) -> int:
+    out = ctypes.c_size_t(0)
+    st = load().pillar_attn_workspace_bytes(ctypes.byref(shape), ctypes.byref(out))
+    if st:
+        raise PillarError("pillar_attn_workspace_bytes", st)
+    return int(out.value)
+
+
+def pillar_attn_unified(shape, q, k_pool, v_pool, slot_table, req_mode, req_len, sparse_idx, sparse_cnt, out,
+                        verify_logits, verify_lse, workspace, stream=None, ws_bytes=None):
+    st = load().pillar_attn_unified(
+        ctypes.byref(shape), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(slot_table), _ptr(req_mode), _ptr(req_len),
+        _ptr(sparse_idx), _ptr(sparse_cnt), _ptr(out), _ptr(verify_logits), _ptr(verify_lse), _ptr(workspace),
+        ws_bytes if ws_bytes is not None else _nbytes(workspace), _stream(stream))
+    if st:
+        raise PillarError("pillar_attn_unified", st)
+
+
+def pillar_topk_workspace_bytes(shape: PillarShape, V: int) -> int:
+    out = ctypes.c_size_t(0)
+    st = load().pillar_topk_workspace_bytes(ctypes.byref(shape), int(V), ctypes.byref(out))
+    if st:
+        raise PillarError("pillar_topk_workspace_bytes", st)
+    return int(out.value)
+
+
+def pillar_topk_select(shape, V, verify_logits, verify_lse, req_len, group_map, K, next_idx, next_cnt, workspace,
+                       stream=None, ws_bytes=None):
+    st = load().pillar_topk_select(
+        ctypes.byref(shape), int(V), _ptr(verify_logits), _ptr(verify_lse), _ptr(req_len), _ptr(group_map), _ptr(K),
+        _ptr(next_idx), _ptr(next_cnt), _ptr(workspace), ws_bytes if ws_bytes is not None else _nbytes(workspace),
+        _stream(stream))
+    if st:
+        raise PillarError("pillar_topk_select", st)
+
+
+def pillar_get_error(workspace, stream=None) -> int:
+    """Synchronise, read and clear the device error word; returns the flags."""
+    flags = ctypes.c_int32(0)
+    st = load().pillar_get_error(_ptr(workspace), _stream(stream), ctypes.byref(flags))
+    if st not in (0, -4):
+        raise PillarError("pillar_get_error", st)
+    return int(flags.value)

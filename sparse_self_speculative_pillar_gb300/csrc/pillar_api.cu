@@ -1,0 +1,182 @@
+// pillar_api.cu -- the C ABI declared in include/pillar.h: argument checks,
+// workspace carving, launches.  Every check that can be made on the host is
+// made here, before anything is enqueued; data-dependent checks are made on
+// the device and reported through the workspace error word.
+#include <cmath>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "pillar_internal.h"
+
+namespace {
+
+using namespace pillar;
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_shape(const pillar_shape_t *s) {
+    if (!s) return PILLAR_ERR_ARG;
+    if (s->B < 0 || s->Hq <= 0 || s->Hkv <= 0 || s->Hq % s->Hkv != 0) return PILLAR_ERR_ARG;
+    const int G = s->Hq / s->Hkv;
+    if (G > kMaxG) return PILLAR_ERR_ARG;
+    if (s->D != 64 && s->D != 128) return PILLAR_ERR_ARG;
+    if (s->k < 0 || (long long)(s->k + 1) * G > kMaxRows) return PILLAR_ERR_ARG;
+    if (s->max_sparse < 0 || s->max_len < 1 || s->num_slots < 1 || s->max_topk < 1) return PILLAR_ERR_ARG;
+    if (s->row_lo < 0 || s->row_hi > s->k + 1 || s->row_lo >= s->row_hi) return PILLAR_ERR_ARG;
+    if (s->reserved != 0) return PILLAR_ERR_ARG;
+    if (!(s->sm_scale >= 0.f) || std::isinf(s->sm_scale)) return PILLAR_ERR_ARG;
+    for (int c : {s->verify_chunk, s->draft_chunk})
+        if (c != 0 && (c < kTileKeys || c > kMaxChunk || c % kTileKeys != 0)) return PILLAR_ERR_ARG;
+    if ((long long)s->B * s->Hkv > (1ll << 30) || (long long)s->max_len * s->Hq * (s->k + 1) > (1ll << 40))
+        return PILLAR_ERR_ARG;
+    return PILLAR_OK;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pillar_attn_workspace_bytes(const pillar_shape_t *shape, size_t *bytes) {
+    const int st = check_shape(shape);
+    if (st != PILLAR_OK) return st;
+    if (!bytes) return PILLAR_ERR_ARG;
+    *bytes = attn_layout(*shape).total;
+    return PILLAR_OK;
+}
+
+int pillar_attn_unified(const pillar_shape_t *shape, const uint16_t *q, const uint16_t *k_pool,
+                        const uint16_t *v_pool, const int32_t *slot_table, const int32_t *req_mode,
+                        const int32_t *req_len, const int32_t *sparse_idx, const int32_t *sparse_cnt,
+                        uint16_t *out, float *verify_logits, float *verify_lse, void *workspace,
+                        size_t ws_bytes, void *stream) {
+    int st = check_shape(shape);
+    if (st != PILLAR_OK) return st;
+    const pillar_shape_t &s = *shape;
+    if (s.B == 0) return PILLAR_OK;
+    if (!q || !k_pool || !v_pool || !slot_table || !req_mode || !req_len || !sparse_cnt || !out ||
+        !verify_logits || !verify_lse)
+        return PILLAR_ERR_ARG;
+    if (s.max_sparse > 0 && !sparse_idx) return PILLAR_ERR_ARG;
+    // bulk copies need 16-byte aligned rows
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 4)) return PILLAR_ERR_ARG;
+    const AttnLayout lay = attn_layout(s);
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < lay.total) return PILLAR_ERR_WORKSPACE;
+    const int nsm = sm_count();
+    if (nsm <= 0) return PILLAR_ERR_CUDA;
+
+    char *ws = static_cast<char *>(workspace);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+
+    PlanArgs pa;
+    pa.req_mode = req_mode;
+    pa.req_len = req_len;
+    pa.sparse_cnt = sparse_cnt;
+    pa.ws = ws;
+    pa.lay = lay;
+    pa.B = s.B;
+    pa.Hq = s.Hq;
+    pa.Hkv = s.Hkv;
+    pa.k = s.k;
+    pa.max_sparse = s.max_sparse;
+    pa.max_len = s.max_len;
+    pa.vchunk = verify_chunk_of(s);
+    pa.dchunk = draft_chunk_of(s);
+    if (launch_plan(pa, cs) != cudaSuccess) return PILLAR_ERR_CUDA;
+
+    AttnArgs aa;
+    aa.q = q;
+    aa.k_pool = k_pool;
+    aa.v_pool = v_pool;
+    aa.slot_table = slot_table;
+    aa.sparse_idx = sparse_idx;
+    aa.out = out;
+    aa.logits = verify_logits;
+    aa.lse = verify_lse;
+    aa.ws = ws;
+    aa.lay = lay;
+    aa.num_slots = s.num_slots;
+    aa.Hq = s.Hq;
+    aa.Hkv = s.Hkv;
+    aa.D = s.D;
+    aa.k = s.k;
+    aa.max_sparse = s.max_sparse;
+    aa.scale = s.sm_scale > 0.f ? s.sm_scale : 1.0f / std::sqrt((float)s.D);
+    if (launch_attn(aa, nsm, cs) != cudaSuccess) return PILLAR_ERR_CUDA;
+    return PILLAR_OK;
+}
+
+int pillar_topk_workspace_bytes(const pillar_shape_t *shape, int32_t V, size_t *bytes) {
+    const int st = check_shape(shape);
+    if (st != PILLAR_OK) return st;
+    if (!bytes || V < 0) return PILLAR_ERR_ARG;
+    *bytes = topk_ws_bytes(*shape, V);
+    return PILLAR_OK;
+}
+
+int pillar_topk_select(const pillar_shape_t *shape, int32_t V, const float *verify_logits,
+                       const float *verify_lse, const int32_t *req_len, const int32_t *group_map,
+                       const int32_t *K, int32_t *next_idx, int32_t *next_cnt, void *workspace,
+                       size_t ws_bytes, void *stream) {
+    int st = check_shape(shape);
+    if (st != PILLAR_OK) return st;
+    if (V < 0) return PILLAR_ERR_ARG;
+    if (V == 0) return PILLAR_OK;
+    if (!verify_logits || !verify_lse || !req_len || !group_map || !K || !next_idx || !next_cnt)
+        return PILLAR_ERR_ARG;
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < topk_ws_bytes(*shape, V)) return PILLAR_ERR_WORKSPACE;
+    if ((long long)V * shape->Hkv > 65535ll * 65535ll || V > 65535) return PILLAR_ERR_ARG;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    TopkArgs ta;
+    ta.logits = verify_logits;
+    ta.lse = verify_lse;
+    ta.req_len = req_len;
+    ta.group_map = group_map;
+    ta.K = K;
+    ta.next_idx = next_idx;
+    ta.next_cnt = next_cnt;
+    ta.ws = static_cast<char *>(workspace);
+    ta.scores = reinterpret_cast<float *>(ta.ws + topk_scores_offset());
+    ta.V = V;
+    ta.Hq = shape->Hq;
+    ta.Hkv = shape->Hkv;
+    ta.k = shape->k;
+    ta.row_lo = shape->row_lo;
+    ta.row_hi = shape->row_hi;
+    ta.max_topk = shape->max_topk;
+    ta.max_len = shape->max_len;
+    if (cudaMemsetAsync(ta.ws, 0, sizeof(int), cs) != cudaSuccess) return PILLAR_ERR_CUDA;
+    if (launch_topk_select(ta, cs) != cudaSuccess) return PILLAR_ERR_CUDA;
+    return PILLAR_OK;
+}
+
+int pillar_get_error(void *workspace, void *stream, int32_t *flags) {
+    if (!workspace || !flags) return PILLAR_ERR_ARG;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return PILLAR_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), cs) != cudaSuccess) return PILLAR_ERR_CUDA;
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return PILLAR_ERR_CUDA;
+    *flags = v;
+    return v ? PILLAR_ERR_DEVICE : PILLAR_OK;
+}
+
+const char *pillar_status_string(int status) {
+    switch (status) {
+        case PILLAR_OK: return "ok";
+        case PILLAR_ERR_ARG: return "bad argument (null pointer, dimension or unsupported shape)";
+        case PILLAR_ERR_WORKSPACE: return "workspace null, misaligned or too small";
+        case PILLAR_ERR_CUDA: return "CUDA runtime or launch error";
+        case PILLAR_ERR_DEVICE: return "device reported an out-of-range index, slot, length or a timeout";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

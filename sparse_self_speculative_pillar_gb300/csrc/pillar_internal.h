@@ -1,0 +1,129 @@
+// pillar_internal.h -- workspace layout and launch constants shared by the
+// planner, the unified attention kernel, the Top-K kernels and the host API.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/pillar.h"
+
+namespace pillar {
+
+constexpr int kTileKeys = 64;          // keys staged per pipeline stage
+constexpr int kConsumerWarps = 4;      // compute warps per CTA
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kMaxRows = 64;           // (k+1)*G bound of a verify tile
+constexpr int kMaxG = 8;               // query heads per KV head
+constexpr int kDefaultVerifyChunk = 1024;
+constexpr int kDefaultDraftChunk = 2048;
+constexpr int kMaxChunk = 4096;        // item key bound (sizes the row list in shared memory)
+constexpr int kPlanThreads = 1024;
+constexpr unsigned long long kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
+
+// Request and unit records written by the planner.
+struct ReqInfo {
+    int q_off;      // first query row
+    int vidx;       // index among verify requests (verify only)
+    int len;        // L_b, clamped to [0, max_len]
+    int mode;       // 0 draft, 1 verify, -1 invalid (skipped)
+};
+
+struct UnitInfo {
+    int nsplit;     // work items of this (request, KV head)
+    int item_base;  // index of its first item
+};
+
+struct Item {
+    int unit;       // b * Hkv + g
+    int begin;      // first key (verify: position; draft: list index)
+    int end;        // one past the last key
+    int split;      // index among the unit's items
+};
+
+struct WsHeader {
+    int err;        // PILLAR_FLAG_* bits
+    int num_items;
+    int item_counter;
+    int num_units;
+    int pad[60];    // keeps the arrays 256-byte aligned
+};
+
+// Byte offsets of the attention workspace sections.
+struct AttnLayout {
+    size_t req, kv_off, logit_off, unit, arrive, items, part_o, part_lse, total;
+    long long max_items;
+    int rows;       // partial row stride: max((k+1)*G, G)
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline int verify_chunk_of(const pillar_shape_t &s) { return s.verify_chunk > 0 ? s.verify_chunk : kDefaultVerifyChunk; }
+inline int draft_chunk_of(const pillar_shape_t &s) { return s.draft_chunk > 0 ? s.draft_chunk : kDefaultDraftChunk; }
+
+inline AttnLayout attn_layout(const pillar_shape_t &s) {
+    AttnLayout l{};
+    const long long B = s.B, U = (long long)s.B * s.Hkv;
+    const int G = s.Hq / s.Hkv;
+    const long long vc = verify_chunk_of(s), dc = draft_chunk_of(s);
+    long long per_unit = (s.max_len + vc - 1) / vc;
+    long long dsplit = (s.max_sparse + dc - 1) / dc;
+    if (dsplit > per_unit) per_unit = dsplit;
+    if (per_unit < 1) per_unit = 1;
+    l.max_items = U * per_unit;
+    l.rows = (s.k + 1) * G > G ? (s.k + 1) * G : G;
+    size_t off = sizeof(WsHeader);
+    l.req = off;       off = align256(off + sizeof(ReqInfo) * B);
+    l.kv_off = off;    off = align256(off + sizeof(long long) * B);
+    l.logit_off = off; off = align256(off + sizeof(long long) * B);
+    l.unit = off;      off = align256(off + sizeof(UnitInfo) * U);
+    l.arrive = off;    off = align256(off + sizeof(int) * U);
+    l.items = off;     off = align256(off + sizeof(Item) * l.max_items);
+    l.part_o = off;    off = align256(off + sizeof(float) * (size_t)l.max_items * l.rows * s.D);
+    l.part_lse = off;  off = align256(off + sizeof(float) * (size_t)l.max_items * l.rows);
+    l.total = off;
+    return l;
+}
+
+// Top-K workspace: header (error word) + packed scores [V][Hkv][L_v].
+inline size_t topk_scores_offset() { return sizeof(WsHeader); }
+inline size_t topk_ws_bytes(const pillar_shape_t &s, int V) {
+    return align256(sizeof(WsHeader) + sizeof(float) * (size_t)V * s.Hkv * (size_t)s.max_len);
+}
+
+// ------------------------------------------------------------------ launchers
+// (host side; each kernel translation unit turns these into its kernel
+// parameters and enqueues on the given stream)
+
+struct PlanArgs {
+    const int *req_mode, *req_len, *sparse_cnt;
+    char *ws;
+    AttnLayout lay;
+    int B, Hq, Hkv, k, max_sparse, max_len, vchunk, dchunk;
+};
+cudaError_t launch_plan(const PlanArgs &a, cudaStream_t st);
+
+struct AttnArgs {
+    const uint16_t *q, *k_pool, *v_pool;
+    const int *slot_table, *sparse_idx;
+    uint16_t *out;
+    float *logits, *lse;
+    char *ws;
+    AttnLayout lay;
+    long long num_slots;
+    int Hq, Hkv, D, k, max_sparse;
+    float scale;
+};
+cudaError_t launch_attn(const AttnArgs &a, int grid, cudaStream_t st);
+
+struct TopkArgs {
+    const float *logits, *lse;
+    const int *req_len, *group_map, *K;
+    int *next_idx, *next_cnt;
+    char *ws;
+    float *scores;
+    int V, Hq, Hkv, k, row_lo, row_hi, max_topk, max_len;
+};
+cudaError_t launch_topk_select(const TopkArgs &a, cudaStream_t st);
+
+}  // namespace pillar

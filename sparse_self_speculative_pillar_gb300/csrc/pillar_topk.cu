@@ -1,0 +1,302 @@
+// pillar_topk.cu -- next critical lists from the verify dump.
+//
+// "SparseSpec-MLSys26", 核心方法 / PillarAttn: the verify kernel dumps logits
+// and LSE; exact softmax scores are rematerialised from them, averaged over
+// the k draft rows and the query heads of one GQA group, and the Top-K
+// positions (K = ceil(s*len)) are the critical set of the next k draft steps.
+//
+//   score[v][g][t] = 1/(R*G) * sum_{r in [row_lo,row_hi)} sum_{h in group g}
+//                    exp(logit[v][h][r][t] - lse[v][h][r])
+//
+// Two kernels:
+//   1. topk_scores: a flat, bandwidth-bound pass over the R*G logit rows of
+//      every (verify request, KV head), 2048 positions per CTA, coalesced
+//      loads; writes fp32 scores (scratch in the workspace, L2-resident for
+//      the next kernel at the usual sizes).
+//   2. topk_select: one CTA per (verify request, KV head): 4-pass 8-bit radix
+//      select of the K-th largest score on the order-preserving uint32 key
+//      of the (non-negative) fp32 score, then an ordered compaction that
+//      keeps everything above the threshold plus the lowest positions equal
+//      to it -- the output comes out ascending with no sort.
+#include "pillar_device.cuh"
+
+namespace pillar {
+
+struct TopkParams {
+    const float *logits, *lse;
+    const int *req_len, *group_map, *K;
+    int *next_idx, *next_cnt;
+    WsHeader *hdr;
+    float *scores;
+    int V, Hq, Hkv, G, k, row_lo, row_hi, max_topk, max_len, smem_keys;
+};
+
+constexpr int kScoreThreads = 256;
+constexpr int kScorePerThread = 8;
+constexpr int kScoreChunk = kScoreThreads * kScorePerThread;
+constexpr int kSelectThreads = 1024;
+constexpr int kSelectSmemKeys = 48 * 1024;  // keys kept in shared memory (192 KB); longer rows stay in global
+
+// Offsets of verify request v in the packed logits (sums over v' < v of
+// Hq*(k+1)*L_v') and in the scores scratch (sums of Hkv*min(L_v', max_len),
+// so that a bad length can never push a later request past the workspace).
+// Every thread of the block gets them.
+__device__ void verify_offsets(const TopkParams &p, int v, long long *lg_off, long long *sc_off) {
+    __shared__ long long red[2][32];
+    long long s = 0, c = 0;
+    for (int i = threadIdx.x; i < v; i += blockDim.x) {
+        const int l = p.req_len[p.group_map[i]];
+        s += l;
+        c += l < 0 ? 0 : (l > p.max_len ? p.max_len : l);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        s += __shfl_xor_sync(0xffffffffu, s, o);
+        c += __shfl_xor_sync(0xffffffffu, c, o);
+    }
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (lane == 0) {
+        red[0][wid] = s;
+        red[1][wid] = c;
+    }
+    __syncthreads();
+    long long ts = 0, tc = 0;
+    for (int w = 0; w < nw; ++w) {
+        ts += red[0][w];
+        tc += red[1][w];
+    }
+    __syncthreads();
+    *lg_off = ts * p.Hq * (p.k + 1);
+    *sc_off = tc * p.Hkv;
+}
+
+__global__ void __launch_bounds__(kScoreThreads) topk_scores_kernel(const TopkParams p) {
+    const int v = blockIdx.z, g = blockIdx.y;
+    const int L = p.req_len[p.group_map[v]];
+    const int t0 = blockIdx.x * kScoreChunk;
+    if (L < 0 || L > p.max_len) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&p.hdr->err, PILLAR_FLAG_REQUEST);
+        return;
+    }
+    if (t0 >= L) return;
+    long long lg_off, sc_off;
+    verify_offsets(p, v, &lg_off, &sc_off);
+    const int R = p.row_hi - p.row_lo, nrows = R * p.G;
+    __shared__ float s_lse[kMaxRows];
+    for (int i = threadIdx.x; i < nrows; i += blockDim.x) {
+        const int h = g * p.G + i / R, r = p.row_lo + i % R;
+        s_lse[i] = p.lse[((long long)v * p.Hq + h) * (p.k + 1) + r];
+    }
+    __syncthreads();
+    float acc[kScorePerThread];
+#pragma unroll
+    for (int e = 0; e < kScorePerThread; ++e) acc[e] = 0.f;
+    for (int i = 0; i < nrows; ++i) {
+        const int h = g * p.G + i / R, r = p.row_lo + i % R;
+        const float *row = p.logits + lg_off + ((long long)h * (p.k + 1) + r) * L;
+        const float ls = s_lse[i];
+        float x[kScorePerThread];
+#pragma unroll
+        for (int e = 0; e < kScorePerThread; ++e) {
+            const int t = t0 + e * kScoreThreads + threadIdx.x;
+            x[e] = t < L ? __ldcs(row + t) : neg_inf();
+        }
+#pragma unroll
+        for (int e = 0; e < kScorePerThread; ++e) acc[e] += expf(x[e] - ls);
+    }
+    const float denom = (float)(R * p.G);
+    float *dst = p.scores + sc_off + (long long)g * L;
+#pragma unroll
+    for (int e = 0; e < kScorePerThread; ++e) {
+        const int t = t0 + e * kScoreThreads + threadIdx.x;
+        if (t < L) dst[t] = acc[e] / denom;
+    }
+}
+
+// Exclusive scan of one int per thread over the select block.
+__device__ int select_block_scan(int v, int *total) {
+    __shared__ int ws[kSelectThreads / 32];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) ws[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int s = ws[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        ws[lane] = s;
+    }
+    __syncthreads();
+    const int base = wid ? ws[wid - 1] : 0;
+    *total = ws[kSelectThreads / 32 - 1];
+    __syncthreads();
+    return base + x - v;
+}
+
+__device__ __forceinline__ uint32_t score_key(float s) { return __float_as_uint(s) & 0x7fffffffu; }
+
+__global__ void __launch_bounds__(kSelectThreads, 1) topk_select_kernel(const TopkParams p) {
+    extern __shared__ uint32_t skeys[];
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t s_prefix, s_mask, s_remaining;
+    const int v = blockIdx.y, g = blockIdx.x, tid = threadIdx.x;
+    const int L = p.req_len[p.group_map[v]];
+    if (L < 0 || L > p.max_len) {
+        if (tid == 0) p.next_cnt[v * p.Hkv + g] = 0;
+        return;
+    }
+    int K = p.K[v];
+    K = K < 0 ? 0 : (K > L ? L : K);
+    if (K > p.max_topk) {
+        if (tid == 0) atomicOr(&p.hdr->err, PILLAR_FLAG_TOPK);
+        K = p.max_topk;
+    }
+    int *dst = p.next_idx + ((long long)v * p.Hkv + g) * p.max_topk;
+    if (tid == 0) p.next_cnt[v * p.Hkv + g] = K;
+    if (K == 0) return;
+    if (K == L) {
+        for (int t = tid; t < L; t += blockDim.x) dst[t] = t;
+        return;
+    }
+    long long lg_off, sc_off;
+    verify_offsets(p, v, &lg_off, &sc_off);
+    const float *sc = p.scores + sc_off + (long long)g * L;
+    const uint32_t *keys;
+    if (L <= p.smem_keys) {
+        for (int t = tid; t < L; t += blockDim.x) skeys[t] = score_key(sc[t]);
+        keys = skeys;
+    } else {
+        keys = reinterpret_cast<const uint32_t *>(sc);  // signless already: scores are >= 0
+    }
+    if (tid == 0) {
+        s_prefix = 0;
+        s_mask = 0;
+        s_remaining = (uint32_t)K;
+    }
+    __syncthreads();
+
+    // Radix select, most significant byte first, of the K-th largest key.
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+        const uint32_t prefix = s_prefix, mask = s_mask;
+        for (int t = tid; t < L; t += blockDim.x) {
+            const uint32_t key = keys[t] & 0x7fffffffu;
+            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (tid < 32) {
+            // lane l owns digits 255-8l .. 248-8l (descending)
+            const uint32_t rem = s_remaining;
+            uint32_t cnt[8], sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                cnt[i] = hist[255 - 8 * tid - i];
+                sum += cnt[i];
+            }
+            uint32_t incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += y;
+            }
+            const uint32_t before = incl - sum;
+            const bool mine = before < rem && incl >= rem;
+            __syncwarp();  // every lane has read s_remaining before it changes
+            if (mine) {
+                uint32_t cum = before;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (cum + cnt[i] >= rem) {
+                        s_prefix = prefix | ((uint32_t)(255 - 8 * tid - i) << shift);
+                        s_mask = mask | (255u << shift);
+                        s_remaining = rem - cum;
+                        break;
+                    }
+                    cum += cnt[i];
+                }
+            }
+        }
+        __syncthreads();
+    }
+    const uint32_t T = s_prefix;
+    const int need_eq = (int)s_remaining;
+
+    // Ordered compaction: each thread owns a contiguous run of positions.
+    const int per = (L + blockDim.x - 1) / blockDim.x;
+    const int tb = min(L, tid * per), te = min(L, tb + per);
+    int cgt = 0, ceq = 0;
+    for (int t = tb; t < te; ++t) {
+        const uint32_t key = keys[t] & 0x7fffffffu;
+        cgt += key > T;
+        ceq += key == T;
+    }
+    int tot_gt, tot_eq;
+    const int gt_before = select_block_scan(cgt, &tot_gt);
+    const int eq_before = select_block_scan(ceq, &tot_eq);
+    int out = gt_before + min(eq_before, need_eq);
+    int eq_rank = eq_before;
+    for (int t = tb; t < te; ++t) {
+        const uint32_t key = keys[t] & 0x7fffffffu;
+        if (key > T) {
+            dst[out++] = t;
+        } else if (key == T) {
+            if (eq_rank < need_eq) dst[out++] = t;
+            ++eq_rank;
+        }
+    }
+}
+
+cudaError_t launch_topk_select(const TopkArgs &a, cudaStream_t st) {
+    TopkParams p;
+    p.logits = a.logits;
+    p.lse = a.lse;
+    p.req_len = a.req_len;
+    p.group_map = a.group_map;
+    p.K = a.K;
+    p.next_idx = a.next_idx;
+    p.next_cnt = a.next_cnt;
+    p.hdr = reinterpret_cast<WsHeader *>(a.ws);
+    p.scores = a.scores;
+    p.V = a.V;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.G = a.Hq / a.Hkv;
+    p.k = a.k;
+    p.row_lo = a.row_lo;
+    p.row_hi = a.row_hi;
+    p.max_topk = a.max_topk;
+    p.max_len = a.max_len;
+    p.smem_keys = min(a.max_len, kSelectSmemKeys);
+    if (p.V == 0) return cudaSuccess;
+    static int configured_mask = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const size_t sel_smem = sizeof(uint32_t) * (size_t)p.smem_keys;
+    const int bit = 1 << (dev & 31);
+    if (!(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & bit)) {
+        e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(sizeof(uint32_t) * kSelectSmemKeys));
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&configured_mask, bit, __ATOMIC_RELEASE);
+    }
+    dim3 g1((p.max_len + kScoreChunk - 1) / kScoreChunk, p.Hkv, p.V);
+    topk_scores_kernel<<<g1, kScoreThreads, 0, st>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    dim3 g2(p.Hkv, p.V);
+    topk_select_kernel<<<g2, kSelectThreads, sel_smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pillar

@@ -1,0 +1,68 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every entry point
+declared in include/pillar.h; host-side argument checks return the
+documented codes without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_self_speculative_pillar_gb300 as P
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "pillar.h")).read()
+    return sorted(set(re.findall(r"PILLAR_API\s+[\w\s\*]*?\b(pillar_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    P.build()
+    return P.load()
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted(P.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_shape_struct_matches_header_layout():
+    # 12 int32, then int64 (8-aligned at 48), float, int32 -> 64 bytes
+    assert ctypes.sizeof(P.PillarShape) == 64
+    assert P.PillarShape.num_slots.offset == 48
+
+
+def _shape(**kw):
+    base = dict(B=4, Hq=32, Hkv=8, D=128, k=8, max_sparse=64, max_len=8192, num_slots=1 << 20, max_topk=410)
+    base.update(kw)
+    return P.make_shape(**base)
+
+
+def test_workspace_sizes_and_argument_checks(lib):
+    n = P.pillar_attn_workspace_bytes(_shape())
+    assert n > 0 and n % 256 == 0
+    assert P.pillar_topk_workspace_bytes(_shape(), 3) >= 3 * 8 * 8192 * 4
+    for bad in (dict(D=96), dict(Hq=30), dict(k=15, Hq=40, Hkv=8), dict(max_len=0), dict(row_lo=3, row_hi=2),
+                dict(verify_chunk=100), dict(draft_chunk=8192), dict(Hq=72, Hkv=8)):
+        with pytest.raises(P.PillarError) as e:
+            P.pillar_attn_workspace_bytes(_shape(**bad))
+        assert e.value.status == -1
+    s = _shape()
+    # null workspace -> -2, with no device work enqueued
+    st = lib.pillar_attn_unified(ctypes.byref(s), *([ctypes.c_void_p(16)] * 11), None, 0, None)
+    assert st == -2
+    # null tensor -> -1
+    st = lib.pillar_attn_unified(ctypes.byref(s), None, *([ctypes.c_void_p(16)] * 10), ctypes.c_void_p(256), 1 << 40,
+                                 None)
+    assert st == -1
+    # B == 0 -> nothing to do
+    s0 = _shape(B=0)
+    assert lib.pillar_attn_unified(ctypes.byref(s0), *([None] * 12), 0, None) == 0
+    assert lib.pillar_topk_select(ctypes.byref(s), 0, *([None] * 8), 0, None) == 0
+    assert P.pillar_status_string(-4).startswith("device")

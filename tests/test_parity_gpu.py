@@ -1,0 +1,269 @@
+"""GPU parity: the sm_103a path, called through the C ABI, against the fp64
+oracle on the same seeded inputs ("SparseSpec-MLSys26", 核心方法 / PillarAttn
+and the unified-batch section define what both compute)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+from tests._gpu_common import Gpu, compare_attn, compare_topk, run_oracle  # noqa: E402
+
+
+def prior_verify_lists(w: W.Workload, seed=7):
+    """Critical lists of each draft request from an oracle verify over its
+    prefix [0, L-p) (k+1 fresh query rows drawn like the workload's), Top-K
+    with K = ceil(s*(L-p)), plus the p positions appended since."""
+    r = w.recipe
+    si = np.zeros((w.B, w.Hkv, w.max_sparse * 2), np.int32)
+    sc = np.zeros((w.B, w.Hkv), np.int32)
+    kvo = w.kv_off
+    kp, vp = w.pool("k"), w.pool("v")
+    for b in range(w.B):
+        if w.req_mode[b] != 0:
+            continue
+        p = int(w.phase[b])
+        L = int(w.req_len[b])
+        Lp = L - p
+        q = W.query_rows(w, w.k + 1, seed + b)
+        res = oracle.attn_unified(Hq=w.Hq, Hkv=w.Hkv, D=w.D, k=w.k, scale=1 / math.sqrt(w.D), q=q, k_pool=kp,
+                                  v_pool=vp, slot_table=w.slot_table[kvo[b]:kvo[b] + Lp],
+                                  req_mode=np.array([1], np.int32), req_len=np.array([Lp], np.int32),
+                                  sparse_idx=np.zeros((1, w.Hkv, 1), np.int32),
+                                  sparse_cnt=np.zeros((1, w.Hkv), np.int32))
+        K = -(-Lp * r.s_num // r.s_den)
+        t = oracle.topk_select(Hq=w.Hq, Hkv=w.Hkv, k=w.k, row_lo=1, row_hi=w.k + 1, logits=res.logits,
+                               lse=oracle.verify_lse_of(res, [1], w.k, w.Hq), L=[Lp], K=[K], max_topk=K)
+        for h in range(w.Hkv):
+            lst = np.concatenate([t.next_idx[0, h, :t.next_cnt[0, h]], np.arange(Lp, L)])
+            si[b, h, :len(lst)] = lst
+            sc[b, h] = len(lst)
+    m = int(sc.max()) if sc.size else 1
+    return si[:, :, :max(m, 1)].copy(), sc
+
+
+def _check(w, g, select=None, sparse_idx=None, sparse_cnt=None):
+    res = g.host()
+    ref = run_oracle(w, select=select, sparse_idx=sparse_idx, sparse_cnt=sparse_cnt)
+    worst = compare_attn(w, res, ref, select=select)
+    return res, ref, worst
+
+
+def test_tiny_workload_with_oracle_critical_lists():
+    """The tiny case exactly as specified: draft lists are the oracle Top-K of a
+    prior verify.  Full elementwise parity, then the GPU Top-K of this step."""
+    w = W.generate("tiny")
+    si, sc = prior_verify_lists(w)
+    w.sparse_idx, w.sparse_cnt = si, sc
+    g = Gpu(w)
+    g.attn()
+    g.topk()
+    assert g.attn_flags() == 0 and g.topk_flags() == 0
+    res, ref, _ = _check(w, g)
+    lse = oracle.verify_lse_of(ref, w.req_mode, w.k, w.Hq)
+    t = oracle.topk_select(Hq=w.Hq, Hkv=w.Hkv, k=w.k, row_lo=1, row_hi=w.k + 1, logits=ref.logits, lse=lse,
+                           L=w.verify_len, K=w.topk_K, max_topk=g.shape.max_topk)
+    compare_topk(res["next_idx"], res["next_cnt"], t, w.verify_len, w.topk_K, w.Hkv)
+
+
+SCALED = [
+    ("qwen3_1p7b", dict(B=20, length_scale=0.1)),
+    ("qwen3_8b", dict(B=19, length_scale=0.05)),
+    ("qwen3_14b", dict(B=11, length_scale=0.03)),
+    ("stress", dict(B=27, length_scale=0.05)),
+    ("stress_all_draft", dict(B=24, length_scale=0.1)),
+    ("stress_all_verify", dict(B=6, length_scale=0.03)),
+]
+
+
+@pytest.mark.parametrize("name,kw", SCALED, ids=[s[0] for s in SCALED])
+def test_scaled_workloads_elementwise(name, kw):
+    """Every output element of reduced-size versions of each workload (many
+    tiles, ragged tails, both modes)."""
+    w = W.generate(W.scaled(name, **kw))
+    g = Gpu(w)
+    g.attn()
+    assert g.attn_flags() == 0
+    _check(w, g)
+
+
+@pytest.mark.parametrize("vchunk,dchunk", [(64, 64), (128, 192), (2048, 2048)])
+def test_split_and_merge_matches_unsplit(vchunk, dchunk):
+    """Forcing many work items per (request, head) exercises the last-arriver
+    LSE merge; results stay within tolerance of the oracle."""
+    w = W.generate(W.scaled("qwen3_8b", B=12, length_scale=0.06, seed_offset=3))
+    g = Gpu(w, verify_chunk=vchunk, draft_chunk=dchunk)
+    g.attn()
+    assert g.attn_flags() == 0
+    _check(w, g)
+
+
+def test_repeated_calls_are_identical():
+    w = W.generate(W.scaled("stress", B=15, length_scale=0.04, seed_offset=5))
+    g = Gpu(w, verify_chunk=128)
+    g.attn()
+    a = g.host()
+    g.out.zero_()
+    g.logits.zero_()
+    g.attn()
+    b = g.host()
+    np.testing.assert_array_equal(a["out"], b["out"])
+    np.testing.assert_array_equal(a["logits"], b["logits"])
+    np.testing.assert_array_equal(a["lse"], b["lse"])
+
+
+def test_topk_isolated_on_gpu_dump():
+    """Top-K alone: the oracle takes the GPU-dumped logits/LSE (fp32 promoted to
+    fp64) and must pick the same sets outside the tie band."""
+    w = W.generate(W.scaled("qwen3_8b", B=28, length_scale=0.2, seed_offset=1))
+    g = Gpu(w)
+    g.attn()
+    g.topk()
+    assert g.topk_flags() == 0
+    res = g.host()
+    t = oracle.topk_select(Hq=w.Hq, Hkv=w.Hkv, k=w.k, row_lo=1, row_hi=w.k + 1, logits=res["logits"],
+                           lse=res["lse"][:w.V], L=w.verify_len, K=w.topk_K, max_topk=g.shape.max_topk)
+    compare_topk(res["next_idx"], res["next_cnt"], t, w.verify_len, w.topk_K, w.Hkv)
+
+
+def test_topk_end_to_end_against_oracle_dump():
+    w = W.generate(W.scaled("qwen3_14b", B=10, length_scale=0.1, seed_offset=2))
+    g = Gpu(w)
+    g.attn()
+    g.topk()
+    res, ref, _ = _check(w, g)
+    t = oracle.topk_select(Hq=w.Hq, Hkv=w.Hkv, k=w.k, row_lo=1, row_hi=w.k + 1, logits=ref.logits,
+                           lse=oracle.verify_lse_of(ref, w.req_mode, w.k, w.Hq), L=w.verify_len, K=w.topk_K,
+                           max_topk=g.shape.max_topk)
+    compare_topk(res["next_idx"], res["next_cnt"], t, w.verify_len, w.topk_K, w.Hkv)
+
+
+def test_chained_verify_topk_then_draft():
+    """A stride on the GPU: verify -> Top-K -> the next step's drafts attend the
+    selected critical lists (plus the newest position)."""
+    w = W.generate(W.scaled("qwen3_1p7b", B=9, length_scale=0.1, seed_offset=4))
+    g = Gpu(w)
+    g.attn()
+    g.topk()
+    res = g.host()
+    # next step: every verify request becomes a draft request over its own lists
+    w2 = W.generate(W.scaled("qwen3_1p7b", B=9, length_scale=0.1, seed_offset=4))
+    si = np.zeros((w.B, w.Hkv, g.shape.max_topk + 1), np.int32)
+    sc = np.zeros((w.B, w.Hkv), np.int32)
+    for v, b in enumerate(w.verify_batch_index):
+        L = int(w.req_len[b])
+        for h in range(w.Hkv):
+            n = int(res["next_cnt"][v, h])
+            lst = res["next_idx"][v, h, :n]
+            if L - 1 not in lst:
+                lst = np.concatenate([lst, [L - 1]])
+            si[b, h, :len(lst)] = lst
+            sc[b, h] = len(lst)
+    w2.req_mode = np.zeros(w.B, np.int32)
+    w2.q = w.q[w.q_off]                    # one query row per request
+    w2.sparse_idx, w2.sparse_cnt = si, sc
+    w2.topk_K = np.zeros(0, np.int32)
+    g2 = Gpu(w2)
+    g2.attn()
+    assert g2.attn_flags() == 0
+    _check(w2, g2)
+
+
+@pytest.mark.parametrize("D,G,k", [(64, 1, 3), (128, 8, 7), (128, 5, 11), (64, 4, 15)])
+def test_shapes(D, G, k):
+    rec = W.scaled("qwen3_8b", B=2 * (k + 1) + 3, length_scale=0.02, seed_offset=10 + D + G + k,
+                   D=D, Hkv=2, Hq=2 * G, k=k)
+    w = W.generate(rec)
+    g = Gpu(w)
+    g.attn()
+    assert g.attn_flags() == 0
+    _check(w, g)
+
+
+def test_edge_lengths_and_lists():
+    """L = 1 draft, single-key and empty lists, a repeated position, verify with
+    L = k+1 and a length that is not a multiple of 64."""
+    rec = W.Recipe("edge", B=6, Hq=8, Hkv=2, D=128, k=3, s_num=1, s_den=20,
+                   lengths=("fixed", [1, 5, 4, 131, 77, 200]), pillar_frac=("fixed", 0.05),
+                   mode_rule="explicit", explicit_modes=(0, 0, 1, 1, 0, 0), explicit_phases=(1, 1, 0, 0, 2, 3),
+                   seed=99)
+    w = W.generate(rec)
+    si = np.zeros((6, 2, 8), np.int32)
+    sc = np.zeros((6, 2), np.int32)
+    si[0, 0, 0] = 0; sc[0, 0] = 1                      # L = 1
+    si[0, 1, 0] = 0; sc[0, 1] = 1
+    si[1, 0, :3] = [4, 0, 4]; sc[1, 0] = 3             # repeated position, unsorted
+    sc[1, 1] = 0                                       # empty list -> zeros
+    si[4, 0, :1] = [76]; sc[4, 0] = 1
+    si[4, 1, :5] = [0, 10, 20, 30, 76]; sc[4, 1] = 5
+    si[5, 0, :8] = np.arange(192, 200); sc[5, 0] = 8
+    si[5, 1, :2] = [199, 3]; sc[5, 1] = 2
+    w.sparse_idx, w.sparse_cnt = si, sc
+    g = Gpu(w)
+    g.attn()
+    assert g.attn_flags() == 0
+    res, ref, _ = _check(w, g)
+    assert np.all(res["out"][w.q_off[1], 4:8] == 0)    # empty list of KV head 1
+
+
+def test_out_of_range_entries_are_flagged_and_skipped():
+    w = W.generate(W.scaled("qwen3_8b", B=4, length_scale=0.02, seed_offset=20))
+    b = int(np.nonzero(w.req_mode == 0)[0][0])
+    L = int(w.req_len[b])
+    n = int(w.sparse_cnt[b, 0])
+    good_idx, good_cnt = w.sparse_idx.copy(), w.sparse_cnt.copy()
+    w.sparse_idx[b, 0, n - 1] = L + 5                  # out-of-range position
+    g = Gpu(w)
+    g.attn()
+    flags = g.attn_flags()
+    assert flags & 1
+    good_cnt[b, 0] = n - 1                             # the oracle without that entry
+    _check(w, g, sparse_idx=good_idx, sparse_cnt=good_cnt)
+
+
+def test_bad_slot_is_flagged():
+    w = W.generate(W.scaled("qwen3_8b", B=4, length_scale=0.02, seed_offset=21))
+    g = Gpu(w)
+    g.slot_table[3] = w.num_slots + 10
+    g.attn()
+    assert g.attn_flags() & 2
+
+
+def test_bad_request_fields_are_flagged():
+    w = W.generate(W.scaled("qwen3_8b", B=4, length_scale=0.02, seed_offset=22))
+    g = Gpu(w)
+    g.req_mode[1] = 7
+    g.attn()
+    assert g.attn_flags() & 4
+
+
+def test_topk_budget_edges_and_ties():
+    """K >= L keeps every position, K = 0 keeps none, K > max_topk is clamped and
+    flagged, and exact ties go to the lower position."""
+    V, Hq, Hkv, k, L = 3, 4, 2, 2, 300
+    lg = np.random.default_rng(5).standard_normal((V, Hq, k + 1, L)).astype(np.float32)
+    lg[0, :, :, 10] = lg[0, :, :, 20] = lg[0, :, :, 30] = 4.0   # identical columns
+    lse = np.log(np.exp(lg.astype(np.float64)).sum(-1)).astype(np.float32)
+    import sparse_self_speculative_pillar_gb300 as P
+    shape = P.make_shape(B=V, Hq=Hq, Hkv=Hkv, D=64, k=k, max_sparse=1, max_len=L, num_slots=1, max_topk=64)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    req_len = dev(np.full(V, L, np.int32))
+    gm = dev(np.arange(V, dtype=np.int32))
+    K = dev(np.array([2, 0, 500], np.int32))
+    nidx = torch.full((V, Hkv, 64), -1, dtype=torch.int32, device="cuda")
+    ncnt = torch.full((V, Hkv), -1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(P.pillar_topk_workspace_bytes(shape, V), dtype=torch.uint8, device="cuda")
+    P.pillar_topk_select(shape, V, dev(lg.ravel()), dev(lse), req_len, gm, K, nidx, ncnt, ws)
+    flags = P.pillar_get_error(ws)
+    assert flags & 32
+    ni, nc = nidx.cpu().numpy(), ncnt.cpu().numpy()
+    assert list(ni[0, 0, :2]) == [10, 20] and list(ni[0, 1, :2]) == [10, 20]
+    assert np.all(nc[1] == 0) and np.all(nc[2] == 64)
+    ref = oracle.topk_select(Hq=Hq, Hkv=Hkv, k=k, row_lo=1, row_hi=k + 1, logits=lg.ravel().astype(np.float64),
+                             lse=lse.astype(np.float64), L=[L] * V, K=[2, 0, 64], max_topk=64)
+    compare_topk(ni, nc, ref, [L] * V, [2, 0, 64], Hkv)

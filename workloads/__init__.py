@@ -316,7 +316,16 @@ def generate(rec: Recipe | str, max_sparse_pad: int = 16) -> Workload:
     Lv = L[mode == 1].astype(np.int64)
     topk_K = np.clip(-(-Lv * rec.s_num // rec.s_den), 1, Lv).astype(np.int32)
     return Workload(rec, mode.astype(np.int32), L, phase, pool, slot_table, q, k_log, v_log,
-                    sparse_idx, sparse_cnt, topk_K, pillar)
+                    sparse_idx, sparse_cnt, topk_K, pillar, extra={"u": u, "pillar_frac": frac})
+
+
+def query_rows(w: Workload, n: int, seed: int) -> np.ndarray:
+    """n extra query tokens [n, Hq, D] (bf16 bits) drawn like the workload's own
+    queries (3*u_h + N(0,1) for the heads of group h)."""
+    g = np.random.default_rng(seed)
+    x = g.standard_normal((n, w.Hq, w.D), dtype=np.float32)
+    x += 3.0 * np.repeat(w.extra["u"], w.G, axis=0)[None, :, :]
+    return f32_to_bf16_bits(x).reshape(n, w.Hq, w.D)
 
 
 def algorithmic_bytes(w: Workload) -> dict:
