@@ -50,6 +50,10 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--length-scale", type=float, default=1.0, help="shorter contexts (profiling runs)")
+    ap.add_argument("--batch", type=int, default=None, help="fewer requests (profiling runs)")
+    ap.add_argument("--quick", action="store_true",
+                    help="headline loop only: no CPU baseline, no breakdown, no end-to-end pass")
     return ap.parse_args()
 
 
@@ -145,48 +149,46 @@ class Clocks:
 
 # --------------------------------------------------------------------------- oracle timing (CPU)
 
-def oracle_sample_time(w, nthreads, budget_s=20.0):
-    """Time the fp64 oracle on a bounded sample of the workload (one verify
-    request of median length, the draft requests next to it, and the Top-K of
-    that verify request) and extrapolate to a full step by algorithmic KV bytes."""
-    import oracle
-    ver = np.nonzero(w.req_mode == 1)[0]
-    dra = np.nonzero(w.req_mode == 0)[0]
-    sel = np.zeros(w.B, bool)
-    vb = ver[np.argsort(w.req_len[ver])[len(ver) // 2]] if len(ver) else None
-    if vb is not None:
-        sel[vb] = True
-    sel[dra[:min(len(dra), 16)]] = True
+def _kv_bytes(w, mask):
     row = w.D * 2 * 2
-    def kv_bytes(mask):
-        vm = mask & (w.req_mode == 1)
-        dm = mask & (w.req_mode == 0)
-        return (int(w.req_len[vm].astype(np.int64).sum()) * w.Hkv * row +
-                int(w.sparse_cnt[dm].astype(np.int64).sum()) * row)
-    total = kv_bytes(np.ones(w.B, bool))
-    samp = kv_bytes(sel)
+    vm = mask & (w.req_mode == 1)
+    dm = mask & (w.req_mode == 0)
+    return (int(w.req_len[vm].astype(np.int64).sum()) * w.Hkv * row +
+            int(w.sparse_cnt[dm].astype(np.int64).sum()) * row)
+
+
+def oracle_step(w, sel, nthreads):
+    """The fp64 oracle over the selected requests of one step: attention, then
+    Top-K of the selected verify requests.  Returns seconds."""
+    import oracle
     t0 = time.perf_counter()
     r = oracle.attn_unified(Hq=w.Hq, Hkv=w.Hkv, D=w.D, k=w.k, scale=1 / math.sqrt(w.D), q=w.q, k_pool=w.k_logical,
                             v_pool=w.v_logical, slot_table=np.arange(len(w.slot_table), dtype=np.int32),
                             req_mode=w.req_mode, req_len=w.req_len, sparse_idx=w.sparse_idx,
                             sparse_cnt=w.sparse_cnt, select=sel, nthreads=nthreads)
-    t_attn = time.perf_counter() - t0
-    t_topk = 0.0
-    if vb is not None:
-        t0 = time.perf_counter()
-        vi = list(ver).index(vb)
+    vsel = [v for v, b in enumerate(w.verify_batch_index) if sel[b]]
+    if vsel:
         oracle.topk_select(Hq=w.Hq, Hkv=w.Hkv, k=w.k, row_lo=1, row_hi=w.k + 1, logits=r.logits,
                            lse=oracle.verify_lse_of(r, w.req_mode, w.k, w.Hq, select=sel),
-                           L=w.verify_len[vi:vi + 1], K=w.topk_K[vi:vi + 1], max_topk=int(w.topk_K[vi]),
+                           L=w.verify_len[vsel], K=w.topk_K[vsel], max_topk=int(w.topk_K[vsel].max()),
                            nthreads=nthreads)
-        t_topk = (time.perf_counter() - t0) * len(ver)   # Top-K cost scales with the verify count
-    scale = total / max(1, samp)
-    est_us = (t_attn * scale + t_topk) * 1e6
-    desc = (f"fp64 oracle on 1 verify request (L={int(w.req_len[vb]) if vb is not None else 0}) + "
-            f"{int(sel.sum()) - (vb is not None)} draft requests of the {w.recipe.name} batch "
-            f"({samp / 1e6:.1f} of {total / 1e6:.1f} MB algorithmic KV) took {t_attn:.2f} s, "
-            f"plus Top-K of that verify request; scaled to the full layer-step by KV bytes")
-    return est_us, desc, t_attn
+    return time.perf_counter() - t0
+
+
+def oracle_baseline(w, nthreads, min_s=10.0, max_s=30.0):
+    """Whole oracle steps of the workload, repeated until about min_s seconds."""
+    sel = np.ones(w.B, bool)
+    times = []
+    t_start = time.perf_counter()
+    while True:
+        times.append(oracle_step(w, sel, nthreads))
+        el = time.perf_counter() - t_start
+        if el >= min_s or el + times[-1] > max_s:
+            break
+    us = statistics.mean(times) * 1e6
+    desc = (f"fp64 oracle, the whole {w.recipe.name} layer-step (attention of all {w.B} requests + Top-K of all "
+            f"{w.V} verify requests) repeated {len(times)} times, {sum(times):.1f} s of CPU work")
+    return us, desc
 
 
 # --------------------------------------------------------------------------- reference arm
@@ -197,26 +199,34 @@ def run_reference(args):
         return 0
     w = W.generate(args.workload)
     nthreads = os.cpu_count() or 1
-    budget = 150.0
-    t_start = time.perf_counter()
-    per_step = []
-    for i in range(args.warmup + args.steps):
-        if time.perf_counter() - t_start > budget and len(per_step) >= 1:
-            break
-        est_us, desc, _ = oracle_sample_time(w, nthreads)
-        if i >= args.warmup or args.steps == 0:
-            per_step.append(est_us)
-        if time.perf_counter() - t_start > budget and per_step:
-            break
-    value = statistics.median(per_step) if per_step else None
+    full = np.ones(w.B, bool)
+    total = _kv_bytes(w, full)
+    t_full = oracle_step(w, full, nthreads)           # calibration, untimed
+    n_all = max(1, args.warmup + args.steps)
+    frac = min(1.0, (150.0 / n_all) / max(t_full, 1e-6))
+    order = np.argsort(-w.req_mode, kind="stable")     # verify requests first, then drafts, in rotation
+    n_req = max(1, int(round(frac * w.B)))
+    per_step, samp_bytes = [], []
+    pos = 0
+    for i in range(n_all):
+        sel = np.zeros(w.B, bool)
+        sel[order[(pos + np.arange(n_req)) % w.B]] = True
+        pos = (pos + n_req) % w.B
+        dt = oracle_step(w, sel, nthreads)
+        if i >= args.warmup:
+            per_step.append(dt)
+            samp_bytes.append(_kv_bytes(w, sel))
+    value = sum(per_step) / max(1, sum(samp_bytes)) * total * 1e6 if per_step else None
+    desc = (f"fp64 oracle; each step computed {n_req} of the {w.B} requests of the {w.recipe.name} batch in "
+            f"rotation (with the Top-K of the verify requests among them); time scaled to the full layer-step "
+            f"by algorithmic KV bytes ({sum(samp_bytes) / 1e6:.0f} MB sampled over {len(per_step)} steps)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3 if value else None,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.recipe.name, "global_batch": int(w.B), "seq_len": int(w.req_len.mean()),
-                   "parallelism": "replicas" if args.gpus > 1 else "single"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
-                         "sample": desc + f"; median over {len(per_step)} timed samples"},
+                   "parallelism": "single"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -239,8 +249,8 @@ def run_gpu(args):
 
     # each rank: its own replica of the workload (distinct seed)
     rec = W.RECIPES[args.workload]
-    if rank:
-        rec = W.scaled(args.workload, seed_offset=1000 * rank)
+    if rank or args.length_scale != 1.0 or args.batch:
+        rec = W.scaled(args.workload, B=args.batch, length_scale=args.length_scale, seed_offset=1000 * rank)
     w = W.generate(rec)
     g = Gpu(w)
     ab = W.algorithmic_bytes(w)
@@ -257,8 +267,7 @@ def run_gpu(args):
     if flags:
         raise RuntimeError(f"device error flags 0x{flags:x} during warm-up")
 
-    # per-call events over the timed region (on the launching stream)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # headline: K steps bracketed by events on the launching stream
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = Clocks(local)
     if world > 1:
@@ -267,25 +276,42 @@ def run_gpu(args):
     clocks.start()
     time.sleep(0.2)
     start.record(stream)
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        g.attn(stream)
-        ev[i][1].record(stream)
-        g.topk(stream)
-        ev[i][2].record(stream)
+    for _ in range(args.steps):
+        step()
     stop.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
     elapsed_ms = start.elapsed_time(stop)
-    attn_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    topk_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     if world > 1:
         t = torch.tensor([elapsed_ms], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         elapsed_ms = float(t.item())
     us_per_step = elapsed_ms * 1e3 / (args.steps * world)
+    if args.quick:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": us_per_step, "unit": UNIT, "n_gpus": world,
+                              "steps": args.steps, "warmup": args.warmup, "quick": True,
+                              "config": {"workload": w.recipe.name, "B": int(w.B)}}), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    # breakdown: the same steps with events around each call (the dominant
+    # call's duration, live, on the launching stream)
+    nb = max(10, min(args.steps, 1000))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nb)]
+    torch.cuda.synchronize()
+    for i in range(nb):
+        ev[i][0].record(stream)
+        g.attn(stream)
+        ev[i][1].record(stream)
+        g.topk(stream)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    attn_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    topk_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
 
     # end to end: per-step inputs from pinned host memory, results back to host
     e2e_steps = args.e2e_steps or max(10, min(args.steps, 500))
@@ -328,7 +354,7 @@ def run_gpu(args):
     traffic = profiled_traffic(w.recipe.name)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        est_us, desc, _ = oracle_sample_time(w, os.cpu_count() or 1)
+        est_us, desc = oracle_baseline(w, os.cpu_count() or 1)
         cpu = {"value": est_us, "unit": UNIT, "cores": os.cpu_count() or 1, "kind": "oracle", "sample": desc}
     line = {
         "metric": METRIC, "value": us_per_step, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -346,12 +372,13 @@ def run_gpu(args):
         "algorithmic_bytes": ab,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "pillar_attn_unified (planner + unified kernel), event-timed per call",
+                     "kernel": "pillar_attn_unified (planner + unified kernel + partial merge), event-timed per call",
                      "peak_kind": peak_kind},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 5 * args.steps,
+        "breakdown_steps": nb,
         "clocks": clk,
         "device_flags": flags,
     }

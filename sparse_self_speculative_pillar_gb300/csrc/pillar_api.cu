@@ -59,7 +59,13 @@ int pillar_attn_unified(const pillar_shape_t *shape, const uint16_t *q, const ui
     int st = check_shape(shape);
     if (st != PILLAR_OK) return st;
     const pillar_shape_t &s = *shape;
-    if (s.B == 0) return PILLAR_OK;
+    if (s.B == 0) {
+        // nothing to compute; a workspace passed in still reads back as clean
+        if (workspace && ws_bytes >= sizeof(WsHeader) &&
+            cudaMemsetAsync(workspace, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return PILLAR_ERR_CUDA;
+        return PILLAR_OK;
+    }
     if (!q || !k_pool || !v_pool || !slot_table || !req_mode || !req_len || !sparse_cnt || !out ||
         !verify_logits || !verify_lse)
         return PILLAR_ERR_ARG;
@@ -127,7 +133,12 @@ int pillar_topk_select(const pillar_shape_t *shape, int32_t V, const float *veri
     int st = check_shape(shape);
     if (st != PILLAR_OK) return st;
     if (V < 0) return PILLAR_ERR_ARG;
-    if (V == 0) return PILLAR_OK;
+    if (V == 0) {
+        if (workspace && ws_bytes >= sizeof(WsHeader) &&
+            cudaMemsetAsync(workspace, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return PILLAR_ERR_CUDA;
+        return PILLAR_OK;
+    }
     if (!verify_logits || !verify_lse || !req_len || !group_map || !K || !next_idx || !next_cnt)
         return PILLAR_ERR_ARG;
     if (!workspace || !aligned(workspace, 256) || ws_bytes < topk_ws_bytes(*shape, V)) return PILLAR_ERR_WORKSPACE;

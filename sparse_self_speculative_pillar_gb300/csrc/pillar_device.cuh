@@ -94,6 +94,17 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2-cached, L1 bypassed).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// One arrival on `bar` once every cp.async this thread issued so far has
+// landed (counts against the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // ---------------------------------------------------------------- tensor-core fragments
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
@@ -119,6 +130,15 @@ __device__ __forceinline__ void mma_bf16_16816(float *c, uint32_t a0, uint32_t a
 }
 
 // ---------------------------------------------------------------- numerics
+
+// Packed fp32 pair FMA (sm_100+): d = a * b + d on both halves.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 d) {
+    unsigned long long ua = *reinterpret_cast<unsigned long long *>(&a);
+    unsigned long long ub = *reinterpret_cast<unsigned long long *>(&b);
+    unsigned long long ud = *reinterpret_cast<unsigned long long *>(&d);
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(ud) : "l"(ua), "l"(ub));
+    return *reinterpret_cast<float2 *>(&ud);
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

@@ -12,12 +12,12 @@ namespace pillar {
 
 constexpr int kTileKeys = 64;          // keys staged per pipeline stage
 constexpr int kConsumerWarps = 4;      // compute warps per CTA
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kThreads = (kConsumerWarps + 2) * 32;  // + a loader warp and a resolver warp
 constexpr int kMaxRows = 64;           // (k+1)*G bound of a verify tile
 constexpr int kMaxG = 8;               // query heads per KV head
 constexpr int kDefaultVerifyChunk = 1024;
-constexpr int kDefaultDraftChunk = 2048;
-constexpr int kMaxChunk = 4096;        // item key bound (sizes the row list in shared memory)
+constexpr int kDefaultDraftChunk = 1024;
+constexpr int kMaxChunk = 1024;        // item key bound (sizes the two row lists in shared memory)
 constexpr int kPlanThreads = 1024;
 constexpr unsigned long long kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
@@ -32,6 +32,8 @@ struct ReqInfo {
 struct UnitInfo {
     int nsplit;     // work items of this (request, KV head)
     int item_base;  // index of its first item
+    int rec_base;   // first partial row of its items (see AttnLayout)
+    int rec_rows;   // partial rows written per item: 4*G (draft), M (split verify) or 0
 };
 
 struct Item {
@@ -46,14 +48,14 @@ struct WsHeader {
     int num_items;
     int item_counter;
     int num_units;
-    int pad[60];    // keeps the arrays 256-byte aligned
+    int num_merge;  // units whose partials the merge kernel combines
+    int pad[59];    // keeps the arrays 256-byte aligned
 };
 
 // Byte offsets of the attention workspace sections.
 struct AttnLayout {
-    size_t req, kv_off, logit_off, unit, arrive, items, part_o, part_lse, total;
-    long long max_items;
-    int rows;       // partial row stride: max((k+1)*G, G)
+    size_t req, kv_off, logit_off, unit, merge_list, items, part_o, part_lse, total;
+    long long max_items, max_rec_rows;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -61,6 +63,9 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline int verify_chunk_of(const pillar_shape_t &s) { return s.verify_chunk > 0 ? s.verify_chunk : kDefaultVerifyChunk; }
 inline int draft_chunk_of(const pillar_shape_t &s) { return s.draft_chunk > 0 ? s.draft_chunk : kDefaultDraftChunk; }
 
+// Partials: a draft item writes one record per consumer warp (4*G rows), a
+// verify item split over several items writes its M = (k+1)*G rows; each
+// partial row is D fp32 values (the normalised output) plus one fp32 LSE.
 inline AttnLayout attn_layout(const pillar_shape_t &s) {
     AttnLayout l{};
     const long long B = s.B, U = (long long)s.B * s.Hkv;
@@ -71,16 +76,18 @@ inline AttnLayout attn_layout(const pillar_shape_t &s) {
     if (dsplit > per_unit) per_unit = dsplit;
     if (per_unit < 1) per_unit = 1;
     l.max_items = U * per_unit;
-    l.rows = (s.k + 1) * G > G ? (s.k + 1) * G : G;
+    const long long per_item = (long long)kConsumerWarps * G > (long long)(s.k + 1) * G ? (long long)kConsumerWarps * G
+                                                                                          : (long long)(s.k + 1) * G;
+    l.max_rec_rows = l.max_items * per_item;
     size_t off = sizeof(WsHeader);
-    l.req = off;       off = align256(off + sizeof(ReqInfo) * B);
-    l.kv_off = off;    off = align256(off + sizeof(long long) * B);
-    l.logit_off = off; off = align256(off + sizeof(long long) * B);
-    l.unit = off;      off = align256(off + sizeof(UnitInfo) * U);
-    l.arrive = off;    off = align256(off + sizeof(int) * U);
-    l.items = off;     off = align256(off + sizeof(Item) * l.max_items);
-    l.part_o = off;    off = align256(off + sizeof(float) * (size_t)l.max_items * l.rows * s.D);
-    l.part_lse = off;  off = align256(off + sizeof(float) * (size_t)l.max_items * l.rows);
+    l.req = off;        off = align256(off + sizeof(ReqInfo) * B);
+    l.kv_off = off;     off = align256(off + sizeof(long long) * B);
+    l.logit_off = off;  off = align256(off + sizeof(long long) * B);
+    l.unit = off;       off = align256(off + sizeof(UnitInfo) * U);
+    l.merge_list = off; off = align256(off + sizeof(int) * U);
+    l.items = off;      off = align256(off + sizeof(Item) * l.max_items);
+    l.part_o = off;     off = align256(off + sizeof(float) * (size_t)l.max_rec_rows * s.D);
+    l.part_lse = off;   off = align256(off + sizeof(float) * (size_t)l.max_rec_rows);
     l.total = off;
     return l;
 }

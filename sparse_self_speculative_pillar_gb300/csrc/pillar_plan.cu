@@ -8,8 +8,13 @@
 // listed first (they are the heavy ones), then draft items, so the work queue
 // is consumed roughly heaviest-first.  The draft/verify mix in one batch is
 // the unified batch of "SparseSpec-MLSys26" (Unified batch scheduler + fused
-// attention kernel); splitting long contexts over CTAs with an LSE merge is
-// this kernel's own load balancing.
+// attention kernel); splitting long contexts over CTAs and merging the pieces
+// by their LSE is this implementation's own load balancing.
+//
+// The planner also places the partial records: every draft item writes one
+// record of G rows per consumer warp, a verify request split over several
+// items writes M = (k+1)*G rows per item; the units that need combining are
+// listed for the merge kernel.
 #include "pillar_device.cuh"
 
 namespace pillar {
@@ -20,7 +25,7 @@ struct PlanParams {
     ReqInfo *req;
     long long *kv_off, *logit_off;
     UnitInfo *unit;
-    int *arrive;
+    int *merge_list;
     Item *items;
     int B, Hq, Hkv, k, max_sparse, max_len, vchunk, dchunk;
 };
@@ -67,8 +72,22 @@ __device__ __forceinline__ int chunking(int n, int chunk, int *ns) {
     return cs;
 }
 
+// Keys, split count and chunk size of unit u (request b = u / Hkv).
+__device__ __forceinline__ int unit_split(const PlanParams &p, const ReqInfo &r, int u, int *n, int *ns, int *bad) {
+    if (r.mode == 1) {
+        *n = r.len;
+        return chunking(r.len, p.vchunk, ns);
+    }
+    int c = r.mode == 0 ? p.sparse_cnt[u] : 0;
+    if (c < 0 || c > p.max_sparse) *bad |= PILLAR_FLAG_COUNT;
+    c = c < 0 ? 0 : (c > p.max_sparse ? p.max_sparse : c);
+    *n = c;
+    return chunking(c, p.dchunk, ns);
+}
+
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     const int tid = threadIdx.x;
+    const int G = p.Hq / p.Hkv, M = (p.k + 1) * G;
     if (tid == 0) {
         p.hdr->err = 0;
         p.hdr->item_counter = 0;
@@ -117,65 +136,76 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     }
     __syncthreads();
 
-    // Units (request, KV head): split counts, then item bases (verify first).
+    // Units (request, KV head): item bases (verify units first), partial-row
+    // bases and the merge list.
     const int U = p.B * p.Hkv;
-    long long cver = 0;
-    for (int pass = 0; pass < 2; ++pass) {
-        long long carry = pass ? cver : 0;
+    long long c_ver_items = 0;
+    {   // pass 0: verify item bases
+        long long carry = 0;
         for (int base = 0; base < U; base += kPlanThreads) {
             const int u = base + tid;
             long long cnt = 0;
-            int ns = 1;
+            int n = 0, ns = 1;
             bool isv = false;
             if (u < U) {
-                const int b = u / p.Hkv;
-                const ReqInfo r = p.req[b];
+                const ReqInfo r = p.req[u / p.Hkv];
+                unit_split(p, r, u, &n, &ns, &bad);
                 isv = r.mode == 1;
-                if (isv) {
-                    chunking(r.len, p.vchunk, &ns);
-                } else {
-                    int n = r.mode == 0 ? p.sparse_cnt[u] : 0;
-                    if (n < 0 || n > p.max_sparse) {
-                        if (pass == 0) bad |= PILLAR_FLAG_COUNT;
-                    }
-                    n = n < 0 ? 0 : (n > p.max_sparse ? p.max_sparse : n);
-                    chunking(n, p.dchunk, &ns);
-                }
-                cnt = (pass == 0) == isv ? ns : 0;
+                cnt = isv ? ns : 0;
             }
             long long tot;
             const long long off = block_exclusive_scan(cnt, &tot);
-            if (u < U && ((pass == 0) == isv)) {
-                UnitInfo ui;
-                ui.nsplit = ns;
-                ui.item_base = (int)(carry + off);
-                p.unit[u] = ui;
-                p.arrive[u] = 0;
-            }
+            if (u < U && isv) p.unit[u].item_base = (int)(carry + off);
             carry += tot;
         }
-        if (pass == 0) cver = carry;
-        else if (tid == 0) {
-            p.hdr->num_items = (int)carry;
-            p.hdr->num_units = U;
+        c_ver_items = carry;
+    }
+    long long c_items = c_ver_items, c_rec = 0, c_merge = 0;
+    for (int base = 0; base < U; base += kPlanThreads) {   // pass 1: the rest
+        const int u = base + tid;
+        long long dcnt = 0, recs = 0, mflag = 0;
+        int n = 0, ns = 1, rec_rows = 0;
+        bool isv = false;
+        if (u < U) {
+            const ReqInfo r = p.req[u / p.Hkv];
+            int dummy = 0;
+            unit_split(p, r, u, &n, &ns, &dummy);
+            isv = r.mode == 1;
+            dcnt = isv ? 0 : ns;
+            rec_rows = isv ? (ns > 1 ? M : 0) : kConsumerWarps * G;
+            recs = (long long)ns * rec_rows;
+            mflag = rec_rows > 0 ? 1 : 0;
         }
+        long long td, tr, tm;
+        const long long od = block_exclusive_scan(dcnt, &td);
+        const long long orr = block_exclusive_scan(recs, &tr);
+        const long long om = block_exclusive_scan(mflag, &tm);
+        if (u < U) {
+            UnitInfo ui;
+            ui.nsplit = ns;
+            ui.item_base = isv ? p.unit[u].item_base : (int)(c_items + od);
+            ui.rec_base = (int)(c_rec + orr);
+            ui.rec_rows = rec_rows;
+            p.unit[u] = ui;
+            if (mflag) p.merge_list[c_merge + om] = u;
+        }
+        c_items += td;
+        c_rec += tr;
+        c_merge += tm;
+    }
+    if (tid == 0) {
+        p.hdr->num_items = (int)c_items;
+        p.hdr->num_units = U;
+        p.hdr->num_merge = (int)c_merge;
     }
     __syncthreads();
 
     // Emit the items.
     for (int u = tid; u < U; u += kPlanThreads) {
-        const int b = u / p.Hkv;
-        const ReqInfo r = p.req[b];
+        const ReqInfo r = p.req[u / p.Hkv];
         const UnitInfo ui = p.unit[u];
-        int n, ns, cs;
-        if (r.mode == 1) {
-            n = r.len;
-            cs = chunking(n, p.vchunk, &ns);
-        } else {
-            n = r.mode == 0 ? p.sparse_cnt[u] : 0;
-            n = n < 0 ? 0 : (n > p.max_sparse ? p.max_sparse : n);
-            cs = chunking(n, p.dchunk, &ns);
-        }
+        int n, ns, dummy = 0;
+        const int cs = unit_split(p, r, u, &n, &ns, &dummy);
         for (int s = 0; s < ns; ++s) {
             Item it;
             it.unit = u;
@@ -198,7 +228,7 @@ cudaError_t launch_plan(const PlanArgs &a, cudaStream_t st) {
     p.kv_off = reinterpret_cast<long long *>(a.ws + a.lay.kv_off);
     p.logit_off = reinterpret_cast<long long *>(a.ws + a.lay.logit_off);
     p.unit = reinterpret_cast<UnitInfo *>(a.ws + a.lay.unit);
-    p.arrive = reinterpret_cast<int *>(a.ws + a.lay.arrive);
+    p.merge_list = reinterpret_cast<int *>(a.ws + a.lay.merge_list);
     p.items = reinterpret_cast<Item *>(a.ws + a.lay.items);
     p.B = a.B;
     p.Hq = a.Hq;
