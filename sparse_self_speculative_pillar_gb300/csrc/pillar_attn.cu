@@ -386,28 +386,70 @@ __device__ bool verify_item(const AttnParams &p, const Ctx &c, int warp, int lan
                     mma_bf16_16816(s[2 * np + 1], a0, a1, a2, a3, b2, b3);
                 }
             }
-            // scale, mask, dump the logits, row maxima
+            // scale, mask, dump the logits, row maxima.  Interior tiles (every key
+            // valid and visible to every row) skip the masking; the dump uses
+            // 8-byte stores when the row offset is even.
             float mx0 = neg_inf(), mx1 = neg_inf();
+            const bool interior = cur.nk == kTileKeys && cur.valid == ~0ull && cur.pos0 + kTileKeys - 1 <= L - kk1;
+            if (interior) {
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
+                for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int key = 8 * nt + c0 + (e & 1);
-                    const int t = cur.pos0 + key;
-                    const bool inkey = key < cur.nk;
-                    const bool kv = inkey && ((cur.valid >> key) & 1ull);
-                    const bool hi = e >= 2;
-                    const bool vis = kv && t <= (hi ? lim1 : lim0);
-                    const float x = vis ? s[nt][e] * p.scale : neg_inf();
-                    s[nt][e] = x;
-                    if (inkey) {
-                        if (!hi && row0 < M) p.logits[lb0 + t] = x;
-                        if (hi && row1 < M) p.logits[lb1 + t] = x;
+                    for (int e = 0; e < 4; ++e) s[nt][e] *= p.scale;
+                    mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+                    mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+                }
+                const long long t0 = cur.pos0 + c0;
+                if (row0 < M) {
+                    float *dst = p.logits + lb0 + t0;
+                    if (((lb0 + t0) & 1) == 0) {
+#pragma unroll
+                        for (int nt = 0; nt < 8; ++nt)
+                            *reinterpret_cast<float2 *>(dst + 8 * nt) = make_float2(s[nt][0], s[nt][1]);
+                    } else {
+#pragma unroll
+                        for (int nt = 0; nt < 8; ++nt) {
+                            dst[8 * nt] = s[nt][0];
+                            dst[8 * nt + 1] = s[nt][1];
+                        }
                     }
-                    if (hi)
-                        mx1 = fmaxf(mx1, x);
-                    else
-                        mx0 = fmaxf(mx0, x);
+                }
+                if (row1 < M) {
+                    float *dst = p.logits + lb1 + t0;
+                    if (((lb1 + t0) & 1) == 0) {
+#pragma unroll
+                        for (int nt = 0; nt < 8; ++nt)
+                            *reinterpret_cast<float2 *>(dst + 8 * nt) = make_float2(s[nt][2], s[nt][3]);
+                    } else {
+#pragma unroll
+                        for (int nt = 0; nt < 8; ++nt) {
+                            dst[8 * nt] = s[nt][2];
+                            dst[8 * nt + 1] = s[nt][3];
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int key = 8 * nt + c0 + (e & 1);
+                        const int t = cur.pos0 + key;
+                        const bool inkey = key < cur.nk;
+                        const bool kv = inkey && ((cur.valid >> key) & 1ull);
+                        const bool hi = e >= 2;
+                        const bool vis = kv && t <= (hi ? lim1 : lim0);
+                        const float x = vis ? s[nt][e] * p.scale : neg_inf();
+                        s[nt][e] = x;
+                        if (inkey) {
+                            if (!hi && row0 < M) p.logits[lb0 + t] = x;
+                            if (hi && row1 < M) p.logits[lb1 + t] = x;
+                        }
+                        if (hi)
+                            mx1 = fmaxf(mx1, x);
+                        else
+                            mx0 = fmaxf(mx0, x);
+                    }
                 }
             }
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));

@@ -92,7 +92,7 @@ def test_scaled_workloads_elementwise(name, kw):
     _check(w, g)
 
 
-@pytest.mark.parametrize("vchunk,dchunk", [(64, 64), (128, 192), (2048, 2048)])
+@pytest.mark.parametrize("vchunk,dchunk", [(64, 64), (128, 192), (1024, 1024)])
 def test_split_and_merge_matches_unsplit(vchunk, dchunk):
     """Forcing many work items per (request, head) exercises the last-arriver
     LSE merge; results stay within tolerance of the oracle."""
