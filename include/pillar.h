@@ -52,6 +52,11 @@ extern "C" {
 #define PILLAR_ERR_WORKSPACE (-2)   /* workspace null, misaligned or too small */
 #define PILLAR_ERR_CUDA (-3)        /* a CUDA runtime call or launch failed */
 #define PILLAR_ERR_DEVICE (-4)      /* pillar_get_error: the device error word is non-zero */
+#define PILLAR_ERR_SCRATCH (-5)     /* pillar_topk_select_noalloc: the shape needs more than its built-in scratch */
+
+/* Size of the scratch array compiled into the library for
+ * pillar_topk_select_noalloc (16 MiB of scores plus a 256-byte header). */
+#define PILLAR_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u + 256u)
 
 /* Bits of the device error word. */
 #define PILLAR_FLAG_INDEX 1         /* a critical-list position outside [0, L_b) was skipped */
@@ -156,6 +161,42 @@ PILLAR_API int pillar_topk_select(const pillar_shape_t *shape, int32_t V, const 
                        const float *verify_lse, const int32_t *req_len, const int32_t *group_map,
                        const int32_t *K, int32_t *next_idx, int32_t *next_cnt, void *workspace,
                        size_t ws_bytes, void *stream);
+
+/*
+ * pillar_topk_select_noalloc -- pillar_topk_select without a workspace.
+ * (The paper has no counterpart: this is a convenience of this library.)
+ *
+ * For callers that cannot allocate device memory themselves -- their HBM is
+ * owned by another allocator (a framework's caching allocator, an inference
+ * server that reserves the whole budget up front), or they sit on a
+ * latency-critical path where cudaMalloc's implicit device synchronisation
+ * is not acceptable.  It computes exactly what pillar_topk_select computes,
+ * with the same kernels; its scratch (error word and fp32 score rows) is one
+ * array of PILLAR_NOALLOC_SCRATCH_BYTES compiled into the library, which
+ * every GPU that loads the library holds until the process exits.  Nothing
+ * is allocated or freed by this call.
+ *
+ *   arguments 1-9   as for pillar_topk_select (inputs and outputs, caller-owned
+ *                   device memory);
+ *   device_flags    NULL or a device int32 that receives the call's device
+ *                   error word (PILLAR_FLAG_* bits) when the call completes.
+ *
+ * Returns PILLAR_ERR_SCRATCH, with nothing enqueued, when the shape needs
+ * more scratch than the array holds (pillar_topk_workspace_bytes(shape, V)
+ * > PILLAR_NOALLOC_SCRATCH_BYTES, about V * Hkv * max_len > 4M scores);
+ * otherwise as pillar_topk_select.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call shares the one array: calls whose work overlaps on
+ * the GPU (different streams, or different host threads on one device) race
+ * on it and must be serialised by the caller.  Each call clears the error
+ * word itself; the score rows are fully rewritten before they are read.
+ */
+PILLAR_API int pillar_topk_select_noalloc(const pillar_shape_t *shape, int32_t V, const float *verify_logits,
+                                          const float *verify_lse, const int32_t *req_len,
+                                          const int32_t *group_map, const int32_t *K, int32_t *next_idx,
+                                          int32_t *next_cnt, int32_t *device_flags, void *stream);
 
 /*
  * pillar_get_error -- synchronises `stream`, then copies the device error

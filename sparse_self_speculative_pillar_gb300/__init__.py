@@ -27,13 +27,14 @@ from . import _build
 __all__ = [
     "PillarShape", "make_shape", "PillarError", "load", "library_path", "build",
     "pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_topk_workspace_bytes",
-    "pillar_topk_select", "pillar_get_error", "pillar_status_string",
+    "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string",
     "FLAG_INDEX", "FLAG_SLOT", "FLAG_REQUEST", "FLAG_COUNT", "FLAG_TIMEOUT", "FLAG_TOPK",
 ]
 
 FLAG_INDEX, FLAG_SLOT, FLAG_REQUEST, FLAG_COUNT, FLAG_TIMEOUT, FLAG_TOPK = 1, 2, 4, 8, 16, 32
 EXPORTED = ("pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_topk_workspace_bytes",
-            "pillar_topk_select", "pillar_get_error", "pillar_status_string")
+            "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string")
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024 + 256
 
 
 class PillarShape(ctypes.Structure):
@@ -92,10 +93,13 @@ def load():
     lib.pillar_attn_unified.argtypes = [SP] + [P] * 11 + [P, ctypes.c_size_t, P]
     lib.pillar_topk_workspace_bytes.argtypes = [SP, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]
     lib.pillar_topk_select.argtypes = [SP, ctypes.c_int32] + [P] * 7 + [P, ctypes.c_size_t, P]
+    lib.pillar_topk_select_noalloc.argtypes = [SP, ctypes.c_int32] + [P] * 8 + [P]
     lib.pillar_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     lib.pillar_status_string.argtypes = [ctypes.c_int]
     lib.pillar_status_string.restype = ctypes.c_char_p
-    for n in EXPORTED[:-1]:
+    for n in EXPORTED:
+        if n == "pillar_status_string":
+            continue
         getattr(lib, n).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -172,6 +176,19 @@ def pillar_topk_select(shape, V, verify_logits, verify_lse, req_len, group_map, 
         _stream(stream))
     if st:
         raise PillarError("pillar_topk_select", st)
+
+
+def pillar_topk_select_noalloc(shape, V, verify_logits, verify_lse, req_len, group_map, K, next_idx, next_cnt,
+                               device_flags=None, stream=None):
+    """pillar_topk_select for callers that cannot allocate device memory: the
+    library's built-in scratch array replaces the workspace.  Calls sharing a
+    device must not overlap on the GPU; the first call on a device should come
+    before any stream capture."""
+    st = load().pillar_topk_select_noalloc(
+        ctypes.byref(shape), int(V), _ptr(verify_logits), _ptr(verify_lse), _ptr(req_len), _ptr(group_map), _ptr(K),
+        _ptr(next_idx), _ptr(next_cnt), _ptr(device_flags), _stream(stream))
+    if st:
+        raise PillarError("pillar_topk_select_noalloc", st)
 
 
 def pillar_get_error(workspace, stream=None) -> int:

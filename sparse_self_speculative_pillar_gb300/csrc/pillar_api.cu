@@ -186,6 +186,7 @@ const char *pillar_status_string(int status) {
         case PILLAR_ERR_WORKSPACE: return "workspace null, misaligned or too small";
         case PILLAR_ERR_CUDA: return "CUDA runtime or launch error";
         case PILLAR_ERR_DEVICE: return "device reported an out-of-range index, slot, length or a timeout";
+        case PILLAR_ERR_SCRATCH: return "shape exceeds the built-in scratch of pillar_topk_select_noalloc";
         default: return "unknown status";
     }
 }
