@@ -22,6 +22,8 @@ int check_shape(const pillar_shape_t *s) {
     if (s->D != 64 && s->D != 128) return PILLAR_ERR_ARG;
     if (s->k < 0 || (long long)(s->k + 1) * G > kMaxRows) return PILLAR_ERR_ARG;
     if (s->max_sparse < 0 || s->max_len < 1 || s->num_slots < 1 || s->max_topk < 1) return PILLAR_ERR_ARG;
+    // the pools are addressed as num_slots * Hkv rows with 32-bit row coordinates
+    if (s->Hkv > 0 && s->num_slots > 0x7fffffffll / s->Hkv) return PILLAR_ERR_ARG;
     if (s->row_lo < 0 || s->row_hi > s->k + 1 || s->row_lo >= s->row_hi) return PILLAR_ERR_ARG;
     if (s->reserved != 0) return PILLAR_ERR_ARG;
     if (!(s->sm_scale >= 0.f) || std::isinf(s->sm_scale)) return PILLAR_ERR_ARG;
@@ -70,7 +72,7 @@ int pillar_attn_unified(const pillar_shape_t *shape, const uint16_t *q, const ui
         !verify_logits || !verify_lse)
         return PILLAR_ERR_ARG;
     if (s.max_sparse > 0 && !sparse_idx) return PILLAR_ERR_ARG;
-    // bulk copies need 16-byte aligned rows
+    // TMA and 16-byte copies need 16-byte aligned rows
     if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 4)) return PILLAR_ERR_ARG;
     const AttnLayout lay = attn_layout(s);
     if (!workspace || !aligned(workspace, 256) || ws_bytes < lay.total) return PILLAR_ERR_WORKSPACE;

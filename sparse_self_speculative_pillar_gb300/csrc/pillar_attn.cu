@@ -13,37 +13,53 @@
 // (same page, "Unified batch scheduler + fused attention kernel": page size 1
 // unifies sparse and full attention in one pipeline).
 //
-// GB300 design: a persistent grid, two CTAs per SM (two independent
-// pipelines per SM), six warps per CTA:
+// GB300 design: a persistent grid of one CTA per SM (the CTA owns the SM's
+// 512 tensor-memory columns and a ring of up to eight 64-key K/V stages in
+// shared memory), ten warps per CTA:
 //   * resolver warp: pops work items from a global atomic counter, reads the
 //     item's records and translates its positions into pool slots (list ->
-//     slot, many independent loads per lane) into one of two row lists, one
-//     item ahead of the loader;
-//   * loader warp: gathers the item's K/V rows into a ring of shared-memory
-//     stages with 16-byte cp.async (a 256-byte page-size-1 row is far too
-//     small a unit for a TMA transfer), completion tracked on the stage's
-//     mbarrier, and bulk-copies the item's query rows; the item's metadata
-//     travels in the stage record, so consumers never read global memory
-//     between items;
-//   * four consumer warps, which never wait on each other: a verify item is a
-//     dense (k+1)*G x 64 tile per stage on the tensor cores (mma.sync bf16 ->
-//     fp32, one 16-row slice per warp, online softmax, logits dumped from the
-//     same accumulators); a draft item runs on the CUDA cores, each warp
-//     taking 16 of the 64 staged keys, each lane owning D/32 dimensions,
-//     sixteen keys reduced at once by a transpose reduction across lanes,
-//     packed fp32x2 FMAs;
-//   * results that need combining -- the four warps' states of a draft item,
-//     the pieces of a verify request split over several items -- are written
-//     as normalised partials (o, lse) and combined afterwards by merge_kernel,
-//     a flat bandwidth pass: o = sum_i e^{lse_i - lse} o_i, lse = log sum_i
-//     e^{lse_i};
+//     slot, many independent loads per lane) into a ring of three row lists,
+//     up to two items ahead of the loaders;
+//   * four loader warps: gather the item's K/V rows into the stage ring with
+//     TMA tile::gather4 (four 256-byte page-size-1 rows per copy) in the
+//     swizzled layout the tensor cores read, completion counted in bytes on
+//     the stage's mbarrier; the item's query rows go to their operand slots
+//     with the first tile and its metadata travels in the stage record.  For
+//     verify items they first prefetch whole slot blocks into L2 (see loader());
+//   * MMA warp (one thread): issues all tensor-core work -- S = Q K^T
+//     (M = 64 query-row slots, N = 64 keys) into one of four S buffers in
+//     tensor memory as soon as a tile has landed, and O += P V with P read
+//     straight from tensor memory once the softmax has written it; a
+//     finished P V releases the stage and the S buffer through
+//     tcgen05.commit, so the tensor pipe runs up to four tiles ahead of the
+//     softmax;
+//   * four consumer warps, for draft and verify items alike.  An item's query
+//     rows (the G heads of a draft token, the (k+1)*G rows of a verify
+//     request) are spread over the four TMEM lane quadrants; each warp reads
+//     its rows with the 16x256b shape, four threads per row, masks (list
+//     validity; for verify rows also causality), dumps the verify logits,
+//     keeps a running maximum and sum, and writes the bf16 probabilities back
+//     over the scores for the P V MMA.  O is rescaled only when a row's
+//     maximum grows by more than 2^8, so the exponentials stay bounded
+//     without touching O on most tiles.  Two items have query operands of
+//     their own (alternating between items) and their O
+//     accumulators sit in separate TMEM columns, so an item's epilogue
+//     overlaps the next item's MMAs;
+//   * a (request, KV head) split over several items (long contexts, long
+//     critical lists) writes normalised partials (o, lse) per item, combined
+//     afterwards by merge_kernel, a flat bandwidth pass:
+//     o = sum_i e^{lse_i - lse} o_i, lse = log sum_i e^{lse_i};
 //   * every wait is bounded (about 1 s); a timeout raises PILLAR_FLAG_TIMEOUT,
-//     the loader waits for its copies still in flight, and the CTA returns.
+//     the loaders wait for their copies still in flight, the MMA thread for
+//     its MMAs, the tensor memory is freed and the CTA returns.
+#include <cuda.h>  // CUtensorMap (the encoder is resolved at run time through the runtime)
+
 #include "pillar_device.cuh"
 
 namespace pillar {
 
 struct AttnParams {
+    CUtensorMap tmap_k, tmap_v;  // the pools as [num_slots * Hkv rows, D] bf16, box 64 x 1, 128-byte swizzle
     const uint16_t *q, *k_pool, *v_pool;
     const int *slot_table, *sparse_idx;
     uint16_t *out;
@@ -57,6 +73,7 @@ struct AttnParams {
     float *part_o, *part_lse;
     long long num_slots;
     int Hq, Hkv, G, k, M, max_sparse;
+    int RQ, RQd;  // query rows per TMEM lane quadrant: verify ceil(M / 4), draft ceil(G / 4)
     float scale;
 };
 
@@ -80,38 +97,56 @@ struct StageMeta {
     int pos0;                  // logical position of key 0 (verify)
     int qb;                    // query buffer of the item
     unsigned long long valid;  // bit i: key i has an in-range position and slot
-    long long pad2;
+    int mode;                  // the item's mode, on every tile
+    int pad;
 };
+
+constexpr int kSBuf = 4;                  // S/P buffers in tensor memory
+constexpr int kRowLists = 3;              // resolved items in flight between the resolver and the loaders
+constexpr int kMaxStages = 8;             // K/V stages in shared memory
+constexpr int kSmemBudget = 227 * 1024;   // dynamic shared memory of one CTA
+constexpr int kMinSmem = 120 * 1024;      // never two CTAs on one SM: each takes all 512 TMEM columns
+constexpr uint32_t kTmemCols = 512;       // 4 S/P buffers x 64 columns, then O of the two query buffers
 
 template <int D>
 struct Smem {
-    static constexpr int KSTR = D * 2 + 16;  // padded row stride: ldmatrix rows hit distinct banks
-    static constexpr int ROWS = kTileKeys * KSTR;
-    static constexpr int STAGE = 2 * ROWS;    // K rows, then V rows
-    static constexpr int NSTAGE = 2;
-    static constexpr int QBUF = kMaxRows * D * 2;
-    static constexpr int off_q = NSTAGE * STAGE;
-    static constexpr int off_rows = off_q + 2 * QBUF;
-    static constexpr int off_info = off_rows + 2 * kMaxChunk * 4;
-    static constexpr int off_meta = off_info + 2 * (int)sizeof(ItemInfo);
-    static constexpr int off_bar = off_meta + NSTAGE * (int)sizeof(StageMeta);
-    static constexpr int NBAR = 2 * NSTAGE + 2 + 4;  // full, empty, qempty[2], rfull[2], rempty[2]
-    static constexpr int off_ps = off_bar + NBAR * 8;
-    static constexpr int off_misc = off_ps + kConsumerWarps * 16 * kMaxG * 4;
-    static constexpr int total = off_misc + 16;
+    static constexpr int KCH = D / 8;              // 16-byte chunks per row
+    static constexpr int CORE_SBO = KCH * 128;     // core-matrix stride along rows (verify Q, K and V tiles)
+    static constexpr int QHALF = 64 * D * 2;       // the 64 query-row slots of one item's S MMA (M = 64)
+    static constexpr int QREG = 2 * QHALF;         // two items' query operands
+    static constexpr int ROWS = kTileKeys * D * 2;  // the K (or V) rows of one tile
+    static constexpr int STAGE = 2 * ROWS;
+    static constexpr int off_q = 0;
+    static constexpr int off_rows = QREG;
+    static constexpr int off_info = off_rows + kRowLists * kMaxChunk * 4;
+    static constexpr int off_meta = off_info + kRowLists * (int)sizeof(ItemInfo);
+    static constexpr int off_pend = off_meta + kMaxStages * (int)sizeof(StageMeta);
+    static constexpr int off_bar = off_pend + kSBuf * 16;
+    // full[8], empty[8], qempty[2], rfull[3], rempty[3], s_full[4], s_free[4], p_full[4], o_free[2], cexit, drain
+    static constexpr int NBAR = 2 * kMaxStages + 2 + 2 * kRowLists + 3 * kSBuf + 2 + 2;
+    static constexpr int off_misc = off_bar + NBAR * 8;
+    static constexpr int off_stage = (off_misc + 16 + 1023) / 1024 * 1024;
+    static constexpr int NSTAGE = (kSmemBudget - off_stage) / STAGE < kMaxStages ? (kSmemBudget - off_stage) / STAGE
+                                                                                 : kMaxStages;
+    static constexpr int used = off_stage + NSTAGE * STAGE;
+    static constexpr int total = used < kMinSmem ? kMinSmem : used;
+    static constexpr uint32_t tO = kSBuf * kTileKeys;  // TMEM column of O for query buffer 0 (+D for buffer 1)
 };
-// two CTAs share an SM's 228 KB
-static_assert(Smem<128>::total <= 113 * 1024, "shared memory budget of two CTAs per SM");
+static_assert(Smem<128>::NSTAGE >= 4 && Smem<64>::NSTAGE >= 4, "stage ring depth");
+static_assert(Smem<128>::total <= kSmemBudget && Smem<64>::total <= kSmemBudget, "shared memory budget");
+static_assert(Smem<128>::tO + 2 * 128 <= kTmemCols, "tensor memory budget");
 static_assert(sizeof(StageMeta) % 16 == 0 && sizeof(ItemInfo) == 64, "record layout");
 
 struct Ctx {
     char *smem;
     StageMeta *meta;
     ItemInfo *iinfo;
-    int *rowlist;  // [2][kMaxChunk]
+    int *rowlist;  // [kRowLists][kMaxChunk]
     uint64_t *full, *empty, *qempty, *rfull, *rempty;
-    float *ps;
+    uint64_t *s_full, *s_free, *p_full, *o_free, *cexit, *drain;
+    int4 *pend;  // [kSBuf] tiles between their S and P V MMAs (MMA thread only)
     volatile int *abort;
+    uint32_t *tmem_slot;
     int *err;
 };
 
@@ -125,22 +160,39 @@ __device__ __forceinline__ Ctx make_ctx(char *smem, const AttnParams &p) {
     c.rowlist = reinterpret_cast<int *>(smem + S::off_rows);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::off_bar);
     c.full = bars;
-    c.empty = bars + S::NSTAGE;
-    c.qempty = bars + 2 * S::NSTAGE;
-    c.rfull = bars + 2 * S::NSTAGE + 2;
-    c.rempty = bars + 2 * S::NSTAGE + 4;
-    c.ps = reinterpret_cast<float *>(smem + S::off_ps);
+    c.empty = bars + kMaxStages;
+    c.qempty = bars + 2 * kMaxStages;
+    c.rfull = c.qempty + 2;
+    c.rempty = c.rfull + kRowLists;
+    c.s_full = c.rempty + kRowLists;
+    c.s_free = c.s_full + kSBuf;
+    c.p_full = c.s_free + kSBuf;
+    c.o_free = c.p_full + kSBuf;
+    c.cexit = c.o_free + 2;
+    c.drain = c.cexit + 1;
+    c.pend = reinterpret_cast<int4 *>(smem + S::off_pend);
     c.abort = reinterpret_cast<volatile int *>(smem + S::off_misc);
+    c.tmem_slot = reinterpret_cast<uint32_t *>(smem + S::off_misc + 4);
     c.err = &p.hdr->err;
     return c;
 }
 
-// Bounded wait that ignores the abort flag: used only to let copies already
-// in flight land before the CTA exits.
+// Bounded wait that ignores the abort flag: used only to let copies or MMAs
+// already in flight finish before the CTA exits.
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
     const unsigned long long t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity))
         if (global_timer_ns() - t0 > kWaitTimeoutNs) return;
+}
+
+// Slot of an item's query row r in the 64-row operand of the S MMA.  With
+// M = 64 the MMA keeps operand row a in TMEM lane 32 (a / 16) + a % 16, so
+// slot 16 q + i lands in lane i of quadrant q: row r goes to quadrant r / RQ,
+// lane r % RQ (RQ <= 16).  The S, P and O rows share those lanes.  Verify row
+// r = j*G + gi, draft row r = gi.
+__device__ __forceinline__ int row_slot(int r, int RQ) {
+    const int q = r / RQ;
+    return 16 * q + (r - q * RQ);
 }
 
 // ============================================================== resolver warp
@@ -148,7 +200,7 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 __device__ void resolver(const AttnParams &p, const Ctx &c, int lane) {
     const int num_items = *reinterpret_cast<volatile int *>(&p.hdr->num_items);
     uint32_t eph = 0;
-    for (int rb = 0;; rb ^= 1) {
+    for (int rb = 0;; rb = rb + 1 == kRowLists ? 0 : rb + 1) {
         if (!mbar_wait(&c.rempty[rb], ((eph >> rb) & 1) ^ 1, c.abort, c.err)) return;
         eph ^= 1u << rb;
         int it = 0;
@@ -221,15 +273,38 @@ __device__ void resolver(const AttnParams &p, const Ctx &c, int lane) {
     }
 }
 
-// ============================================================== loader warp
+// ============================================================== loader warps
 
+// The loader warps share every tile: warp li fetches rows [RW li, RW li + RW),
+// RW = 64 / kLoaderWarps, of K and of V by TMA tile::gather4 (four rows per
+// copy, each lane issuing its own) into the 128-byte-swizzled layout the
+// tensor cores read, split in 64-column halves; each announces its bytes on
+// the stage barrier.  All loaders run the same deterministic sequence; loader
+// 0 also stages the query rows (16-byte cp.async) and writes the stage record.
+// At the start of a verify item each loader prefetches into L2 whole slot
+// blocks (all KV heads of a position, Hkv*D*2 contiguous bytes of K and of
+// V) for the positions p = g (mod Hkv): verify items are ordered request,
+// chunk, head, so the Hkv CTAs working on one chunk run side by side and
+// each fetches an Hkv-th of the blocks for all of them.  The pool's 256-byte
+// head rows then come from L2; HBM sees whole-block reads, which it serves
+// far faster than scattered 256-byte ones.
 template <int D>
-__device__ void loader(const AttnParams &p, const Ctx &c, int lane) {
+__device__ void loader(const AttnParams &p, const Ctx &c, int lane, int li) {
     using S = Smem<D>;
+    constexpr int NH = D / 64;                  // 64-column halves of a row
+    constexpr int RW = kTileKeys / kLoaderWarps;  // rows of a tile per loader warp
+    constexpr int GW = RW / 4;                  // gather4 row groups per loader warp
+    static_assert(GW * 2 * NH <= 32, "one gather4 per lane");
     int stage = 0, qn = 0;
     uint32_t phase = 0, qph = 0, fph = 0, issued = 0, issued_par = 0;
     bool ok = true;
-    for (int rb = 0;; rb ^= 1) {
+    const char *kpool = reinterpret_cast<const char *>(p.k_pool);
+    const char *vpool = reinterpret_cast<const char *>(p.v_pool);
+    const uint32_t block_bytes = (uint32_t)p.Hkv * D * 2;
+    // this lane's gather4: row group rgl of the warp's rows, K (kv 0) or V (kv 1), column half h
+    const int rgl = lane % GW, kv = (lane / GW) & 1, h = lane / (2 * GW);
+    const bool gl = h < NH;
+    for (int rb = 0;; rb = rb + 1 == kRowLists ? 0 : rb + 1) {
         ok = mbar_wait(&c.rfull[rb], (fph >> rb) & 1, c.abort, c.err);
         if (!ok) break;
         fph ^= 1u << rb;
@@ -237,10 +312,10 @@ __device__ void loader(const AttnParams &p, const Ctx &c, int lane) {
         if (info.it < 0) {
             ok = mbar_wait(&c.empty[stage], phase ^ 1, c.abort, c.err);
             if (ok) {
-                cp_async_arrive_noinc(&c.full[stage]);
+                if (li == 0) cp_async_arrive_noinc(&c.full[stage]);
                 __syncwarp();
                 if (lane == 0) {
-                    c.meta[stage].flags = kStop;
+                    if (li == 0) c.meta[stage].flags = kStop;
                     mbar_arrive(&c.full[stage]);
                 }
             }
@@ -251,14 +326,24 @@ __device__ void loader(const AttnParams &p, const Ctx &c, int lane) {
         const int n = info.n, g = info.g;
         const int ntiles = n > 0 ? (n + kTileKeys - 1) / kTileKeys : 1;
         const int qb = qn & 1;  // two query buffers: this item's may still hold the one before last
+        ++qn;
+        if (verify) {  // this CTA's share of the chunk's slot blocks, into L2
+            const int i0 = ((g - info.begin) % p.Hkv + p.Hkv) % p.Hkv;
+            for (int i = i0 + p.Hkv * (li * 32 + lane); i < n; i += p.Hkv * 32 * kLoaderWarps) {
+                const int sl = rows[i];
+                if (sl >= 0) {
+                    bulk_prefetch_l2(kpool + (size_t)sl * block_bytes, block_bytes);
+                    bulk_prefetch_l2(vpool + (size_t)sl * block_bytes, block_bytes);
+                }
+            }
+        }
         for (int t = 0; t < ntiles; ++t) {
             ok = mbar_wait(&c.empty[stage], phase ^ 1, c.abort, c.err);
             if (!ok) break;
-            if (t == 0) {
+            if (t == 0 && li == 0) {
                 ok = mbar_wait(&c.qempty[qb], ((qph >> qb) & 1) ^ 1, c.abort, c.err);
                 if (!ok) break;
                 qph ^= 1u << qb;
-                ++qn;
             }
             const int k0 = t * kTileKeys;
             const int nk = max(0, min(kTileKeys, n - k0));
@@ -267,55 +352,54 @@ __device__ void loader(const AttnParams &p, const Ctx &c, int lane) {
             const unsigned v0 = __ballot_sync(0xffffffffu, r0 >= 0);
             const unsigned v1 = __ballot_sync(0xffffffffu, r1 >= 0);
             const unsigned long long valid = ((unsigned long long)v1 << 32) | v0;
-            // Keys that are invalid or past the tail still get a real row (the
-            // first valid key's): every staged row then holds finite pool data
-            // and a zero probability can never meet a NaN.
-            int fb = 0;
-            if (valid) {
-                const int f = __ffsll((long long)valid) - 1;
-                fb = __shfl_sync(0xffffffffu, f < 32 ? r0 : r1, f & 31);
+            if (lane == 0) {
+                if (li == 0) {  // the stage record
+                    StageMeta &m = c.meta[stage];
+                    if (t == 0) m.info = info;
+                    m.nk = nk;
+                    m.flags = (t == 0 ? kFirst : 0) | (t == ntiles - 1 ? kLast : 0);
+                    m.pos0 = verify ? info.begin + k0 : 0;
+                    m.qb = qb;
+                    m.valid = valid;
+                    m.mode = info.mode;
+                }
+                mbar_arrive_expect_tx(&c.full[stage], valid ? (uint32_t)(RW * D * 2 * 2) : 0u);  // this warp's rows of K and V
             }
-            char *sK = c.smem + stage * S::STAGE;
-            char *sV = sK + S::ROWS;
+            __syncwarp();
             if (valid) {
-                // 16-byte cp.async: D/8 lanes per row, 256/D rows per warp pass
-                constexpr int LPR = D / 8, RPP = 32 / LPR;
-                const int cch = lane % LPR, rsub = lane / LPR;
-                const int s0 = r0 >= 0 ? r0 : fb, s1 = r1 >= 0 ? r1 : fb;
-                const char *kpool = reinterpret_cast<const char *>(p.k_pool);
-                const char *vpool = reinterpret_cast<const char *>(p.v_pool);
-#pragma unroll 4
-                for (int i = 0; i < kTileKeys / RPP; ++i) {
-                    const int row = RPP * i + rsub;  // the rows of one pass lie on the same side of 32
-                    const int sl = __shfl_sync(0xffffffffu, row < 32 ? s0 : s1, row & 31);
-                    const size_t off = ((size_t)sl * p.Hkv + g) * (D * 2) + cch * 16;
-                    cp_async16(sK + row * S::KSTR + cch * 16, kpool + off);
-                    cp_async16(sV + row * S::KSTR + cch * 16, vpool + off);
+                // Keys that are invalid or past the tail still get a real row (the
+                // first valid key's): every staged row then holds finite pool data
+                // and a zero probability can never meet a NaN.
+                const int f = __ffsll((long long)valid) - 1;
+                const int fb = __shfl_sync(0xffffffffu, f < 32 ? r0 : r1, f & 31);
+                const int sown = (RW * li < 32) ? (r0 >= 0 ? r0 : fb) : (r1 >= 0 ? r1 : fb);
+                int rr[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = RW * li + 4 * rgl + e;  // the warp's rows lie on one side of 32
+                    rr[e] = __shfl_sync(0xffffffffu, sown, i & 31) * p.Hkv + g;
+                }
+                if (gl) {
+                    char *dst = c.smem + S::off_stage + stage * S::STAGE + kv * S::ROWS + h * (kTileKeys * 128) +
+                                (RW * li + 4 * rgl) * 128;
+                    tma_gather4(dst, kv ? (const void *)&p.tmap_v : (const void *)&p.tmap_k, 64 * h, rr[0], rr[1], rr[2],
+                                rr[3], &c.full[stage]);
                 }
             }
-            cp_async_arrive_noinc(&c.full[stage]);  // lands with this lane's copies
-            __syncwarp();
-            const int qrows = verify ? p.k + 1 : 1;
-            const uint32_t qbytes = (uint32_t)p.G * D * 2;
-            if (lane == 0) {
-                StageMeta &m = c.meta[stage];
-                if (t == 0) m.info = info;
-                m.nk = nk;
-                m.flags = (t == 0 ? kFirst : 0) | (t == ntiles - 1 ? kLast : 0);
-                m.pos0 = verify ? info.begin + k0 : 0;
-                m.qb = qb;
-                m.valid = valid;
-                if (t == 0)
-                    mbar_arrive_expect_tx(&c.full[stage], (uint32_t)qrows * qbytes);
-                else
-                    mbar_arrive(&c.full[stage]);
-            }
-            __syncwarp();
-            if (t == 0) {
-                char *qdst = c.smem + S::off_q + qb * S::QBUF;
-                for (int j = lane; j < qrows; j += 32)
-                    bulk_g2s(qdst + j * qbytes, p.q + ((size_t)(info.q_off + j) * p.Hq + (size_t)g * p.G) * D, qbytes,
-                             &c.full[stage]);
+            if (li == 0) {
+                if (t == 0) {  // query rows into their operand slots, core-matrix layout
+                    char *qreg = c.smem + S::off_q + qb * S::QHALF;
+                    const int nchunks = (verify ? p.M : p.G) * S::KCH;
+                    const int rq = verify ? p.RQ : p.RQd;
+                    for (int i = lane; i < nchunks; i += 32) {
+                        const int r = i / S::KCH, cc = i - r * S::KCH;
+                        const int j = verify ? r / p.G : 0, gi = r - j * p.G;
+                        const int a = row_slot(r, rq);
+                        cp_async16(qreg + (a >> 3) * S::CORE_SBO + cc * 128 + (a & 7) * 16,
+                                   p.q + ((size_t)(info.q_off + j) * p.Hq + (size_t)g * p.G + gi) * D + cc * 8);
+                    }
+                }
+                cp_async_arrive_noinc(&c.full[stage]);  // lands with this lane's query copies (if any)
             }
             issued |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
@@ -330,474 +414,481 @@ __device__ void loader(const AttnParams &p, const Ctx &c, int lane) {
     }
     if (!ok) {
         // Let every copy this warp started land before the CTA can exit.
-        for (int s = 0; s < S::NSTAGE; ++s)
-            if ((issued >> s) & 1) drain_wait(&c.full[s], (issued_par >> s) & 1);
+        for (int s2 = 0; s2 < S::NSTAGE; ++s2)
+            if ((issued >> s2) & 1) drain_wait(&c.full[s2], (issued_par >> s2) & 1);
     }
 }
 
-// ============================================================== verify items (tensor cores)
+// ============================================================== MMA warp
 
+// One thread issues every tensor-core operation of the CTA.  It walks the
+// stage ring in order and keeps two cursors: vs, the next tile whose
+// S = Q K^T to issue (needs the tile landed and its S buffer released by the
+// P V four tiles back), and vp, the next tile whose O += P V to issue (needs
+// the softmax's P, and for an item's first tile its O columns read out by the
+// epilogue two items back).
+// Both are polled with non-blocking tests, so neither waits behind the other.
 template <int D>
-__device__ bool verify_item(const AttnParams &p, const Ctx &c, int warp, int lane, int &stage, uint32_t &phase,
-                            StageMeta cur) {
+__device__ void mma_issuer(const AttnParams &p, const Ctx &c, uint32_t tbase) {
     using S = Smem<D>;
-    const ItemInfo in = cur.info;
-    const int G = p.G, M = p.M, kk1 = p.k + 1, L = in.L, g = in.g;
-    const bool active = warp * 16 < M;
-    const int row0 = warp * 16 + (lane >> 2), row1 = row0 + 8;
-    const int j0 = row0 / G, gi0 = row0 - j0 * G, j1 = row1 / G, gi1 = row1 - j1 * G;
-    const int lim0 = L - kk1 + j0, lim1 = L - kk1 + j1;
-    const long long lb0 = in.logit_off + ((long long)(g * G + gi0) * kk1 + j0) * L;
-    const long long lb1 = in.logit_off + ((long long)(g * G + gi1) * kk1 + j1) * L;
-    const int c0 = 2 * (lane & 3);
-
-    // Query rows stay in this item's shared-memory buffer; each tile reloads
-    // the warp's A fragments from it (rows >= M read as zero).
-    const int qb = cur.qb;
-    const uint32_t qaddr = smem_u32(c.smem + S::off_q + qb * S::QBUF) +
-                           (uint32_t)(min(warp * 16 + (lane & 7) + (((lane >> 3) & 1) << 3), kMaxRows - 1) * D * 2 +
-                                      (lane >> 4) * 16);
-
-    float o[D / 8][4];
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
-
-    for (;;) {
-        if (active && cur.valid) {
-            const uint32_t kb = smem_u32(c.smem + stage * S::STAGE);
-            const uint32_t vb = kb + S::ROWS;
-            float s[8][4];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-            // S = Q K^T over the 64 staged keys
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(qaddr + ks * 32, a0, a1, a2, a3);
-                if (row0 >= M) a0 = a2 = 0u;
-                if (row1 >= M) a1 = a3 = 0u;
-#pragma unroll
-                for (int np = 0; np < 4; ++np) {
-                    uint32_t b0, b1, b2, b3;
-                    const int key = 16 * np + ((lane >> 4) << 3) + (lane & 7);
-                    ldsm_x4(kb + key * S::KSTR + (2 * ks + ((lane >> 3) & 1)) * 16, b0, b1, b2, b3);
-                    mma_bf16_16816(s[2 * np], a0, a1, a2, a3, b0, b1);
-                    mma_bf16_16816(s[2 * np + 1], a0, a1, a2, a3, b2, b3);
-                }
-            }
-            // scale, mask, dump the logits, row maxima.  Interior tiles (every key
-            // valid and visible to every row) skip the masking; the dump uses
-            // 8-byte stores when the row offset is even.
-            float mx0 = neg_inf(), mx1 = neg_inf();
-            const bool interior = cur.nk == kTileKeys && cur.valid == ~0ull && cur.pos0 + kTileKeys - 1 <= L - kk1;
-            if (interior) {
-#pragma unroll
-                for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) s[nt][e] *= p.scale;
-                    mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-                    mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
-                }
-                const long long t0 = cur.pos0 + c0;
-                if (row0 < M) {
-                    float *dst = p.logits + lb0 + t0;
-                    if (((lb0 + t0) & 1) == 0) {
-#pragma unroll
-                        for (int nt = 0; nt < 8; ++nt)
-                            *reinterpret_cast<float2 *>(dst + 8 * nt) = make_float2(s[nt][0], s[nt][1]);
-                    } else {
-#pragma unroll
-                        for (int nt = 0; nt < 8; ++nt) {
-                            dst[8 * nt] = s[nt][0];
-                            dst[8 * nt + 1] = s[nt][1];
-                        }
-                    }
-                }
-                if (row1 < M) {
-                    float *dst = p.logits + lb1 + t0;
-                    if (((lb1 + t0) & 1) == 0) {
-#pragma unroll
-                        for (int nt = 0; nt < 8; ++nt)
-                            *reinterpret_cast<float2 *>(dst + 8 * nt) = make_float2(s[nt][2], s[nt][3]);
-                    } else {
-#pragma unroll
-                        for (int nt = 0; nt < 8; ++nt) {
-                            dst[8 * nt] = s[nt][2];
-                            dst[8 * nt + 1] = s[nt][3];
-                        }
-                    }
-                }
+    constexpr uint32_t idS = umma_idesc_bf16(64, kTileKeys, 0, 0);  // M = 64 query-row slots
+    constexpr uint32_t idO = umma_idesc_bf16(64, D, 0, 1);
+    const uint32_t sq0 = smem_u32(c.smem + S::off_q);
+    int stage = 0;
+    uint32_t phase = 0, vs = 0, vp = 0;
+    uint32_t ocount0 = 0, ocount1 = 0;  // items finished per query buffer (scalars: no local-memory array)
+    bool stopped = false, started = false, issued = false;
+    unsigned long long t_idle = 0;
+    for (uint32_t spin = 0;; ++spin) {
+        bool progress = false;
+        if (!stopped && vs - vp < (uint32_t)kSBuf && mbar_test_wait(&c.full[stage], phase)) {
+            const StageMeta &m = c.meta[stage];
+            const int flags = m.flags;
+            bool advance = false;
+            if (flags & kStop) {
+                stopped = true;
             } else {
+                const uint32_t sb = vs % kSBuf;
+                if (mbar_test_wait(&c.s_free[sb], ((vs / kSBuf) & 1) ^ 1)) {
+                    fence_proxy_async_smem();  // cp.async data seen through the stage barrier -> tensor-core reads
+                    tc_fence_after();
+                    const int qb = m.qb;
+                    const int valid = m.valid != 0ull;
+                    if (valid) {
+                        const uint32_t sk = smem_u32(c.smem + S::off_stage + stage * S::STAGE);
+                        const uint32_t sq = sq0 + qb * S::QHALF;
 #pragma unroll
-                for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int key = 8 * nt + c0 + (e & 1);
-                        const int t = cur.pos0 + key;
-                        const bool inkey = key < cur.nk;
-                        const bool kv = inkey && ((cur.valid >> key) & 1ull);
-                        const bool hi = e >= 2;
-                        const bool vis = kv && t <= (hi ? lim1 : lim0);
-                        const float x = vis ? s[nt][e] * p.scale : neg_inf();
-                        s[nt][e] = x;
-                        if (inkey) {
-                            if (!hi && row0 < M) p.logits[lb0 + t] = x;
-                            if (hi && row1 < M) p.logits[lb1 + t] = x;
-                        }
-                        if (hi)
-                            mx1 = fmaxf(mx1, x);
-                        else
-                            mx0 = fmaxf(mx0, x);
+                        for (int ks = 0; ks < D / 16; ++ks)  // K: 64-column halves of 8 KB, 32 bytes per K step
+                            umma_bf16(tbase + sb * kTileKeys, umma_sdesc(sq + ks * 256, 128, S::CORE_SBO),
+                                      umma_sdesc_sw128(sk + (ks >> 2) * (kTileKeys * 128) + (ks & 3) * 32, 16, 1024), idS,
+                                      ks > 0 ? 1u : 0u);
                     }
+                    umma_commit(&c.s_full[sb]);
+                    if (flags & kLast) {  // the item's query rows are free once its last S has completed
+                        mbar_arrive_cnt(&c.qempty[qb], kConsumerWarps - 1);
+                        umma_commit(&c.qempty[qb]);
+                    }
+                    c.pend[sb] = make_int4(stage, qb, flags, valid);  // (shared memory: no local-memory stack)
+                    ++vs;
+                    issued = true;
+                    advance = true;
                 }
             }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-            const float u0 = n0 == neg_inf() ? 0.f : n0, u1 = n1 == neg_inf() ? 0.f : n1;
-            const float a0 = exp2f((m0 - u0) * kLog2e), a1 = exp2f((m1 - u1) * kLog2e);
-            m0 = n0;
-            m1 = n1;
-            float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                s[nt][0] = exp2f((s[nt][0] - u0) * kLog2e);
-                s[nt][1] = exp2f((s[nt][1] - u0) * kLog2e);
-                s[nt][2] = exp2f((s[nt][2] - u1) * kLog2e);
-                s[nt][3] = exp2f((s[nt][3] - u1) * kLog2e);
-                ls0 += s[nt][0] + s[nt][1];
-                ls1 += s[nt][2] + s[nt][3];
+            if (advance && ++stage == S::NSTAGE) {
+                stage = 0;
+                phase ^= 1;
             }
-            l0 = l0 * a0 + ls0;
-            l1 = l1 * a1 + ls1;
+            progress = advance || stopped;
+        }
+        if (vp < vs) {
+            const uint32_t sb = vp % kSBuf;
+            const int4 pe = c.pend[sb];  // stage, query buffer, flags, valid of the tile
+            const int e_stage = pe.x, e_qb = pe.y, e_flags = pe.z, e_valid = pe.w;
+            bool ready = mbar_test_wait(&c.p_full[sb], (vp / kSBuf) & 1);
+            if (ready && (e_flags & kFirst))
+                ready = mbar_test_wait(&c.o_free[e_qb], ((e_qb ? ocount1 : ocount0) & 1) ^ 1);
+            if (ready) {
+                tc_fence_after();
+                if (e_valid) {
+                    const uint32_t sv = smem_u32(c.smem + S::off_stage + e_stage * S::STAGE + S::ROWS);
+                    const uint32_t tO = tbase + S::tO + (uint32_t)e_qb * D;
 #pragma unroll
-            for (int i = 0; i < D / 8; ++i) {
-                o[i][0] *= a0;
-                o[i][1] *= a0;
-                o[i][2] *= a1;
-                o[i][3] *= a1;
-            }
-            // O += P V
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint32_t pa0 = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-                const uint32_t pa1 = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-                const uint32_t pa2 = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-                const uint32_t pa3 = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-                const int key = 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
-#pragma unroll
-                for (int dp = 0; dp < D / 16; ++dp) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(vb + key * S::KSTR + (2 * dp + (lane >> 4)) * 16, b0, b1, b2, b3);
-                    mma_bf16_16816(o[2 * dp], pa0, pa1, pa2, pa3, b0, b1);
-                    mma_bf16_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
+                    for (int ks = 0; ks < kTileKeys / 16; ++ks)
+                        umma_bf16_ts(tO, tbase + sb * kTileKeys + ks * 8,  // V: 16 keys = two 8-key atoms
+                                     umma_sdesc_sw128(sv + ks * 2048, kTileKeys * 128, 1024), idO,
+                                     (started || ks > 0) ? 1u : 0u);
+                    started = true;
                 }
+                umma_commit(&c.s_free[sb]);      // S/P buffer free, and the O of this tile final
+                umma_commit(&c.empty[e_stage]);  // K and V rows consumed
+                if (e_flags & kLast) {
+                    started = false;
+                    if (e_qb) ++ocount1; else ++ocount0;
+                }
+                ++vp;
+                progress = true;
             }
         }
-        mbar_arrive(&c.empty[stage]);
-        const bool last = cur.flags & kLast;
-        if (++stage == S::NSTAGE) {
-            stage = 0;
-            phase ^= 1;
+        if (stopped && vp == vs) break;
+        if (progress) {
+            t_idle = 0;
+            continue;
         }
-        if (last) break;
-        if (!mbar_wait(&c.full[stage], phase, c.abort, c.err)) return false;
-        cur = c.meta[stage];
-    }
-
-    mbar_arrive(&c.qempty[qb]);  // done with this item's query rows
-
-    // Epilogue: normalise; write the output (or the item's partial) and the LSE.
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
-    const float e0 = l0 > 0.f ? m0 + logf(l0) : neg_inf();
-    const float e1 = l1 > 0.f ? m1 + logf(l1) : neg_inf();
-    if (active) {
-        if (in.nsplit == 1) {
-            const size_t or0 = ((size_t)(in.q_off + j0) * p.Hq + (size_t)g * G + gi0) * D;
-            const size_t or1 = ((size_t)(in.q_off + j1) * p.Hq + (size_t)g * G + gi1) * D;
-#pragma unroll
-            for (int dn = 0; dn < D / 8; ++dn) {
-                const int d = 8 * dn + c0;
-                if (row0 < M)
-                    *reinterpret_cast<uint32_t *>(p.out + or0 + d) = pack_bf16x2(o[dn][0] * i0, o[dn][1] * i0);
-                if (row1 < M)
-                    *reinterpret_cast<uint32_t *>(p.out + or1 + d) = pack_bf16x2(o[dn][2] * i1, o[dn][3] * i1);
-            }
-            if ((lane & 3) == 0) {
-                if (row0 < M) p.lse[((size_t)in.vidx * p.Hq + (size_t)g * G + gi0) * kk1 + j0] = e0;
-                if (row1 < M) p.lse[((size_t)in.vidx * p.Hq + (size_t)g * G + gi1) * kk1 + j1] = e1;
-            }
-        } else {
-            const size_t pr0 = (size_t)in.rec + row0, pr1 = (size_t)in.rec + row1;
-#pragma unroll
-            for (int dn = 0; dn < D / 8; ++dn) {
-                const int d = 8 * dn + c0;
-                if (row0 < M)
-                    *reinterpret_cast<float2 *>(p.part_o + pr0 * D + d) = make_float2(o[dn][0] * i0, o[dn][1] * i0);
-                if (row1 < M)
-                    *reinterpret_cast<float2 *>(p.part_o + pr1 * D + d) = make_float2(o[dn][2] * i1, o[dn][3] * i1);
-            }
-            if ((lane & 3) == 0) {
-                if (row0 < M) p.part_lse[pr0] = e0;
-                if (row1 < M) p.part_lse[pr1] = e1;
+        __nanosleep(20);  // idle: leave the issue slots to the warps sharing this sub-partition
+        if ((spin & 63) == 0) {
+            if (*c.abort) break;
+            const unsigned long long now = global_timer_ns();
+            if (t_idle == 0) {
+                t_idle = now;
+            } else if (now - t_idle > kWaitTimeoutNs) {
+                atomicOr(c.err, PILLAR_FLAG_TIMEOUT);
+                *c.abort = 1;
+                break;
             }
         }
     }
-    return true;
+    if (issued) {  // every MMA issued has completed before the tensor memory can be freed
+        umma_commit(c.drain);
+        drain_wait(c.drain, 0);
+    }
 }
 
-// ============================================================== draft items (CUDA cores)
+// ============================================================== consumer warps
 
-// Sixteen per-lane partial sums v[0..16) (one per key) are reduced across the
-// 32 lanes so that every lane ends with the full sum of key lane >> 1: each
-// butterfly stage sends half of the lane's values to its partner and keeps
-// the other half -- 16 shuffles for 16 keys instead of 5 per key.
-__device__ __forceinline__ float transpose_reduce16(float (&v)[16], int lane) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const bool up = lane & 16;
-        const float send = up ? v[i] : v[i + 8], keep = up ? v[i + 8] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+// Consumer state that persists across items.
+struct CState {
+    int stage;
+    uint32_t phase;
+    uint32_t vt;      // tiles this CTA has processed (selects S buffers and barrier parities)
+    uint32_t tbase;   // TMEM base address
+};
+
+constexpr float kRescaleLog2 = 8.f;  // O is rescaled once a row maximum has grown by more than 2^8
+
+// One query row of an item as seen by one of the four threads that share it.
+struct VRow {
+    bool act;
+    int row, j, gi, lim;
+    long long lb;   // offset of the row's logits at position 0 (verify)
+    float m, l;     // reference maximum of P, and the sum of this thread's probabilities
+};
+
+// Row i of the warp's quadrant: verify row r = j*G + gi sees positions up to
+// L-(k+1)+j; a draft row r = gi sees every listed position.
+__device__ __forceinline__ VRow item_row(const AttnParams &p, const ItemInfo &in, bool verify, int warp, int i) {
+    VRow r;
+    const int rq = verify ? p.RQ : p.RQd;
+    r.row = warp * rq + i;
+    r.act = i < rq && r.row < (verify ? p.M : p.G);
+    r.j = 0;
+    r.gi = r.row;
+    r.lim = 0x7fffffff;
+    r.lb = 0;
+    r.m = neg_inf();
+    r.l = 0.f;
+    if (r.act && verify) {
+        const int kk1 = p.k + 1;
+        r.j = r.row / p.G;
+        r.gi = r.row - r.j * p.G;
+        r.lim = in.L - kk1 + r.j;
+        r.lb = in.logit_off + ((long long)(in.g * p.G + r.gi) * kk1 + r.j) * in.L;
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const bool up = lane & 8;
-        const float send = up ? v[i] : v[i + 4], keep = up ? v[i + 4] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const bool up = lane & 4;
-        const float send = up ? v[i] : v[i + 2], keep = up ? v[i + 2] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
-    {
-        const bool up = lane & 2;
-        const float send = up ? v[0] : v[1], keep = up ? v[1] : v[0];
-        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-    }
-    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+    return r;
 }
 
-// This lane's D/32 bf16 elements of a shared-memory row, as fp32 pairs.
-template <int D>
-__device__ __forceinline__ void load_dims(const char *row, int lane, float2 (&x)[D / 64]) {
-    if constexpr (D == 128) {
-        const uint2 w = *reinterpret_cast<const uint2 *>(row + lane * 8);
-        x[0] = make_float2(bf16lo(w.x), bf16hi(w.x));
-        x[1] = make_float2(bf16lo(w.y), bf16hi(w.y));
+// This thread's 16 scores of one row (chunk c, pair e <-> key 8c + cq + e,
+// held in s[4c + OFF + e]): scale, mask, dump the logits of verify rows;
+// returns their max.
+template <int OFF>
+__device__ __forceinline__ float row_scores(const AttnParams &p, const StageMeta &cur, const VRow &r, float *s, int cq,
+                                            bool verify) {
+    if (!r.act) return neg_inf();
+    const bool interior = cur.nk == kTileKeys && cur.valid == ~0ull && cur.pos0 + kTileKeys - 1 <= r.lim;
+    if (interior) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) s[4 * c + OFF + e] *= p.scale;
     } else {
-        const uint32_t w = *reinterpret_cast<const uint32_t *>(row + lane * 4);
-        x[0] = make_float2(bf16lo(w), bf16hi(w));
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int key = 8 * c + cq + e;
+                const bool vis = key < cur.nk && ((cur.valid >> key) & 1ull) && cur.pos0 + key <= r.lim;
+                s[4 * c + OFF + e] = vis ? s[4 * c + OFF + e] * p.scale : neg_inf();
+            }
+    }
+    // maximum as a tree (short dependency chains)
+    float m8[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) m8[c] = fmaxf(s[4 * c + OFF], s[4 * c + OFF + 1]);
+#pragma unroll
+    for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int c = 0; c < w; ++c) m8[c] = fmaxf(m8[c], m8[c + w]);
+    const float mt = m8[0];
+    if (!verify) return mt;
+    // the row's four threads write 8 consecutive positions per chunk
+    float *dst = p.logits + r.lb + cur.pos0 + cq;
+    if (cur.nk == kTileKeys) {
+        if (((r.lb + cur.pos0) & 1) == 0) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<float2 *>(dst + 8 * c) = make_float2(s[4 * c + OFF], s[4 * c + OFF + 1]);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                dst[8 * c] = s[4 * c + OFF];
+                dst[8 * c + 1] = s[4 * c + OFF + 1];
+            }
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                if (8 * c + cq + e < cur.nk) dst[8 * c + e] = s[4 * c + OFF + e];
+    }
+    return mt;
+}
+
+// Probabilities of one row as bf16 pairs (P column 4c + t%4 <-> keys 8c + cq, +1).
+template <int OFF>
+__device__ __forceinline__ void row_probs(VRow &r, const float *s, uint32_t *pw) {
+    if (r.act) {
+        const float nb = -(r.m == neg_inf() ? 0.f : r.m) * kLog2e;
+        float l8[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float p0 = ex2_approx(fmaf(s[4 * c + OFF], kLog2e, nb));
+            const float p1 = ex2_approx(fmaf(s[4 * c + OFF + 1], kLog2e, nb));
+            l8[c] = p0 + p1;
+            pw[2 * c + OFF / 2] = pack_bf16x2(p0, p1);
+        }
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int c = 0; c < w; ++c) l8[c] += l8[c + w];
+        r.l += l8[0];
+    } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) pw[2 * c + OFF / 2] = 0u;
     }
 }
 
-template <int D, int GMAX>
-__device__ bool draft_item(const AttnParams &p, const Ctx &c, int warp, int lane, int &stage, uint32_t &phase,
-                           StageMeta cur) {
-    using S = Smem<D>;
-    constexpr int NP = D / 64;                 // fp32 pairs per lane (D/32 dimensions)
-    constexpr int HC = GMAX < 4 ? GMAX : 4;    // heads reduced together
-    const ItemInfo in = cur.info;
-    const int G = p.G;
+// The normalised output of one row from this thread's O columns (c0 + 8c + cq, +1).
+template <int D, int OFF>
+__device__ __forceinline__ void row_output(const AttnParams &p, const ItemInfo &in, const VRow &r, const float *ov, int c0,
+                                           int cq, float inv) {
+    if (!r.act) return;
+    if (in.nsplit == 1) {
+        uint16_t *dst = p.out + ((size_t)(in.q_off + r.j) * p.Hq + (size_t)in.g * p.G + r.gi) * D + c0 + cq;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint32_t *>(dst + 8 * c) = pack_bf16x2(ov[4 * c + OFF] * inv, ov[4 * c + OFF + 1] * inv);
+    } else {
+        float *dst = p.part_o + ((size_t)in.rec + r.row) * D + c0 + cq;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float2 *>(dst + 8 * c) = make_float2(ov[4 * c + OFF] * inv, ov[4 * c + OFF + 1] * inv);
+    }
+}
 
-    float2 qf[GMAX][NP];
-    {
-        const char *qbuf = c.smem + S::off_q + cur.qb * S::QBUF;
-#pragma unroll
-        for (int h = 0; h < GMAX; ++h) {
-            if (h < G) {
-                load_dims<D>(qbuf + h * D * 2, lane, qf[h]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < NP; ++e) qf[h][e] = make_float2(0.f, 0.f);
-            }
-        }
-    }
-    mbar_arrive(&c.qempty[cur.qb]);
-    float2 o[GMAX][NP];
-    float mw[GMAX], lp[GMAX];
-#pragma unroll
-    for (int h = 0; h < GMAX; ++h) {
-        mw[h] = neg_inf();
-        lp[h] = 0.f;
-#pragma unroll
-        for (int e = 0; e < NP; ++e) o[h][e] = make_float2(0.f, 0.f);
-    }
-    float *ps = c.ps + warp * 16 * kMaxG;   // [16 keys][kMaxG] probabilities of this warp's keys
-    const int key_l = lane >> 1;
+// The consumer side of an item.  The warp reads lanes 0-15 of
+// its TMEM quadrant with the 16x256b shape: each row (lane) is shared by four
+// threads, sixteen columns each; thread t holds rows t/4 ("A") and 8 + t/4
+// ("B", present when a quadrant holds more than eight rows).
+template <int D>
+__device__ bool attn_item(const AttnParams &p, const Ctx &c, int warp, int lane, CState &cs, StageMeta cur) {
+    using S = Smem<D>;
+    const ItemInfo in = cur.info;
+    const bool verify = in.mode == 1;
+    const int qb = cur.qb;
+    const int cq = 2 * (lane & 3);
+    VRow ra = item_row(p, in, verify, warp, lane >> 2);
+    VRow rb = item_row(p, in, verify, warp, 8 + (lane >> 2));
+    const bool have_b = (verify ? p.RQ : p.RQd) > 8;  // warp-uniform
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;  // lanes 0-15 of the warp's quadrant (M = 64)
+    const uint32_t tO = cs.tbase + S::tO + (uint32_t)qb * D;
+    uint32_t last_vt = 0;
 
     for (;;) {
-        if (cur.valid) {
-            const char *sK = c.smem + stage * S::STAGE + (16 * warp) * S::KSTR;
-            const char *sV = sK + S::ROWS;
-            const int key = 16 * warp + key_l;
-            const bool kv = key < cur.nk && ((cur.valid >> key) & 1ull);
-            float sv[GMAX];
-#pragma unroll
-            for (int hc = 0; hc < GMAX; hc += HC) {
-                if (hc < G) {
-                    float part[HC][16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        float2 kf[NP];
-                        load_dims<D>(sK + j * S::KSTR, lane, kf);
-#pragma unroll
-                        for (int h = 0; h < HC; ++h) {
-                            float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-                            for (int e = 0; e < NP; ++e) a = ffma2(qf[hc + h][e], kf[e], a);
-                            part[h][j] = a.x + a.y;
-                        }
-                    }
-#pragma unroll
-                    for (int h = 0; h < HC; ++h) {
-                        const float d = transpose_reduce16(part[h], lane);
-                        sv[hc + h] = kv ? d * p.scale : neg_inf();
-                    }
-                } else {
-#pragma unroll
-                    for (int h = 0; h < HC; ++h) sv[hc + h] = neg_inf();
-                }
-            }
-            // online softmax over this warp's 16 keys (lane pairs hold the same key)
-#pragma unroll
-            for (int h = 0; h < GMAX; ++h) {
-                if (h < G) {
-                    float mt = sv[h];
-                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
-                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
-                    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-                    const float mn = fmaxf(mw[h], mt);
-                    const float mu = mn == neg_inf() ? 0.f : mn;
-                    const float a = exp2f((mw[h] - mu) * kLog2e);
-                    mw[h] = mn;
-                    const float pr = exp2f((sv[h] - mu) * kLog2e);
-                    lp[h] = lp[h] * a + ((lane & 1) ? 0.f : pr);
-#pragma unroll
-                    for (int e = 0; e < NP; ++e) o[h][e] = make_float2(o[h][e].x * a, o[h][e].y * a);
-                    if ((lane & 1) == 0) ps[key_l * kMaxG + h] = pr;
-                }
-            }
-            __syncwarp();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                float2 vf[NP];
-                load_dims<D>(sV + j * S::KSTR, lane, vf);
-                float pj[GMAX];
-                if constexpr (GMAX >= 4) {
-#pragma unroll
-                    for (int h4 = 0; h4 < GMAX; h4 += 4) {
-                        const float4 w4 = *reinterpret_cast<const float4 *>(ps + j * kMaxG + h4);
-                        pj[h4] = w4.x;
-                        pj[h4 + 1] = w4.y;
-                        pj[h4 + 2] = w4.z;
-                        pj[h4 + 3] = w4.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int h = 0; h < GMAX; ++h) pj[h] = ps[j * kMaxG + h];
-                }
-#pragma unroll
-                for (int h = 0; h < GMAX; ++h) {
-                    if (h < G) {
-                        const float2 pp = make_float2(pj[h], pj[h]);
-#pragma unroll
-                        for (int e = 0; e < NP; ++e) o[h][e] = ffma2(pp, vf[e], o[h][e]);
-                    }
-                }
-            }
-            __syncwarp();  // the probabilities are rewritten by the next tile
+        const uint32_t vt = cs.vt, sb = vt % kSBuf;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.empty[cs.stage]);  // the stage is read by the tensor cores only
+        if (!mbar_wait(&c.s_full[sb], (vt / kSBuf) & 1, c.abort, c.err)) return false;
+        tc_fence_after();
+        const uint32_t tS = cs.tbase + sb * kTileKeys;
+        float s[32];
+        tmem_ld16x256b_x8(tS + lane_base, s);
+        float mta = row_scores<0>(p, cur, ra, s, cq, verify);
+        float mtb = have_b ? row_scores<2>(p, cur, rb, s, cq, verify) : neg_inf();
+        mta = fmaxf(mta, __shfl_xor_sync(0xffffffffu, mta, 1));
+        mta = fmaxf(mta, __shfl_xor_sync(0xffffffffu, mta, 2));
+        if (have_b) {
+            mtb = fmaxf(mtb, __shfl_xor_sync(0xffffffffu, mtb, 1));
+            mtb = fmaxf(mtb, __shfl_xor_sync(0xffffffffu, mtb, 2));
         }
-        mbar_arrive(&c.empty[stage]);
+        // running maxima: rescale O only when one grows by more than 2^8
+        const float mna = fmaxf(ra.m, mta), mnb = fmaxf(rb.m, mtb);
+        const bool grow_a = ra.act && ra.m != neg_inf() && (mna - ra.m) * kLog2e > kRescaleLog2;
+        const bool grow_b = rb.act && rb.m != neg_inf() && (mnb - rb.m) * kLog2e > kRescaleLog2;
+        const float aa = grow_a ? exp2f((ra.m - mna) * kLog2e) : 1.f;
+        const float ab = grow_b ? exp2f((rb.m - mnb) * kLog2e) : 1.f;
+        if (grow_a) {
+            ra.l *= aa;
+            ra.m = mna;
+        }
+        if (grow_b) {
+            rb.l *= ab;
+            rb.m = mnb;
+        }
+        if (ra.act && ra.m == neg_inf()) ra.m = mna;  // first visible keys of the row
+        if (rb.act && rb.m == neg_inf()) rb.m = mnb;
+        // P (bf16 pairs) over the scores, for the P V MMA
+        uint32_t pw[16];
+        row_probs<0>(ra, s, pw);
+        if (have_b) {
+            row_probs<2>(rb, s, pw);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) pw[2 * q + 1] = 0u;
+        }
+        if (__any_sync(0xffffffffu, grow_a || grow_b)) {
+            // O holds this item's earlier tiles (a grow needs one): the last P V must have completed
+            const uint32_t pv = vt - 1;
+            if (!mbar_wait(&c.s_free[pv % kSBuf], (pv / kSBuf) & 1, c.abort, c.err)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 64) {
+                float ov[32];
+                tmem_ld16x256b_x8(tO + lane_base + c0, ov);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    ov[4 * q] *= aa;
+                    ov[4 * q + 1] *= aa;
+                    ov[4 * q + 2] *= ab;
+                    ov[4 * q + 3] *= ab;
+                }
+                tmem_st16x256b_x8(tO + lane_base + c0, ov);
+            }
+        }
+        tmem_st16x128b_x8(tS + lane_base, pw);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.p_full[sb]);
+        last_vt = vt;
+        cs.vt = vt + 1;
         const bool last = cur.flags & kLast;
-        if (++stage == S::NSTAGE) {
-            stage = 0;
-            phase ^= 1;
+        if (++cs.stage == S::NSTAGE) {
+            cs.stage = 0;
+            cs.phase ^= 1;
         }
         if (last) break;
-        if (!mbar_wait(&c.full[stage], phase, c.abort, c.err)) return false;
-        cur = c.meta[stage];
+        if (!mbar_wait(&c.full[cs.stage], cs.phase, c.abort, c.err)) return false;
+        cur = c.meta[cs.stage];
     }
 
-    // This warp's partial: normalised over its own keys, with its LSE.
-    const size_t rec = (size_t)in.rec + (size_t)warp * G;
+    // epilogue: the item's last P V has completed
+    if (!mbar_wait(&c.s_free[last_vt % kSBuf], (last_vt / kSBuf) & 1, c.abort, c.err)) return false;
+    tc_fence_after();
+    ra.l += __shfl_xor_sync(0xffffffffu, ra.l, 1);
+    ra.l += __shfl_xor_sync(0xffffffffu, ra.l, 2);
+    rb.l += __shfl_xor_sync(0xffffffffu, rb.l, 1);
+    rb.l += __shfl_xor_sync(0xffffffffu, rb.l, 2);
+    const float inva = ra.l > 0.f ? 1.f / ra.l : 0.f, invb = rb.l > 0.f ? 1.f / rb.l : 0.f;
 #pragma unroll
-    for (int h = 0; h < GMAX; ++h) {
-        if (h < G) {
-            float l = lp[h];
+    for (int c0 = 0; c0 < D; c0 += 64) {
+        float ov[32];
+        tmem_ld16x256b_x8(tO + lane_base + c0, ov);  // warp-collective: every lane loads
+        row_output<D, 0>(p, in, ra, ov, c0, cq, inva);
+        if (have_b) row_output<D, 2>(p, in, rb, ov, c0, cq, invb);
+    }
+    if ((lane & 3) == 0 && (verify || in.nsplit > 1)) {
+        const int kk1 = p.k + 1;
 #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            float2 *dst = reinterpret_cast<float2 *>(p.part_o + (rec + h) * D + lane * (D / 32));
-#pragma unroll
-            for (int e = 0; e < NP; ++e) dst[e] = make_float2(o[h][e].x * inv, o[h][e].y * inv);
-            if (lane == 0) p.part_lse[rec + h] = l > 0.f ? mw[h] + logf(l) : neg_inf();
+        for (int h = 0; h < 2; ++h) {
+            const VRow &r = h ? rb : ra;
+            if (!r.act) continue;
+            const float lse = r.l > 0.f ? r.m + logf(r.l) : neg_inf();
+            if (in.nsplit == 1)
+                p.lse[((size_t)in.vidx * p.Hq + (size_t)in.g * p.G + r.gi) * kk1 + r.j] = lse;
+            else
+                p.part_lse[(size_t)in.rec + r.row] = lse;
         }
     }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c.o_free[qb]);
     return true;
+}
+
+template <int D>
+__device__ void consumer(const AttnParams &p, const Ctx &c, int warp, int lane, uint32_t tbase) {
+    CState cs;
+    cs.stage = 0;
+    cs.phase = 0;
+    cs.vt = 0;
+    cs.tbase = tbase;
+    for (;;) {
+        if (!mbar_wait(&c.full[cs.stage], cs.phase, c.abort, c.err)) break;
+        const StageMeta m = c.meta[cs.stage];
+        if (m.flags & kStop) break;
+        if (!attn_item<D>(p, c, warp, lane, cs, m)) break;
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.cexit);
 }
 
 // ============================================================== kernel
 
-template <int D, int GMAX>
-__device__ void consumer(const AttnParams &p, const Ctx &c, int warp, int lane) {
-    int stage = 0;
-    uint32_t phase = 0;
-    for (;;) {
-        if (!mbar_wait(&c.full[stage], phase, c.abort, c.err)) return;
-        const StageMeta m = c.meta[stage];
-        if (m.flags & kStop) return;
-        const bool ok = m.info.mode == 1 ? verify_item<D>(p, c, warp, lane, stage, phase, m)
-                                         : draft_item<D, GMAX>(p, c, warp, lane, stage, phase, m);
-        if (!ok) return;
-    }
-}
-
-template <int D, int GMAX>
-__global__ void __launch_bounds__(kThreads, 2) unified_attn_kernel(const AttnParams p) {
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) unified_attn_kernel(const __grid_constant__ AttnParams p) {
     extern __shared__ __align__(1024) char smem[];
     using S = Smem<D>;
     const Ctx c = make_ctx<D>(smem, p);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S::NSTAGE; ++s) {
-            mbar_init(&c.full[s], 32 + 1);  // the loader lanes' copy arrivals + its metadata arrival
-            mbar_init(&c.empty[s], kConsumerWarps * 32);
+            mbar_init(&c.full[s], kLoaderWarps + 32);  // one byte-count arrival per loader + loader 0's query-copy arrivals
+            mbar_init(&c.empty[s], kConsumerWarps + 1);    // one per consumer warp + the MMA thread
         }
-        mbar_init(&c.qempty[0], kConsumerWarps * 32);
-        mbar_init(&c.qempty[1], kConsumerWarps * 32);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&c.rfull[i], 32);
-            mbar_init(&c.rempty[i], 32);
+            mbar_init(&c.qempty[i], kConsumerWarps);
+            mbar_init(&c.o_free[i], kConsumerWarps);
         }
+        for (int i = 0; i < kRowLists; ++i) {
+            mbar_init(&c.rfull[i], 32);
+            mbar_init(&c.rempty[i], kLoaderWarps * 32);
+        }
+        for (int i = 0; i < kSBuf; ++i) {
+            mbar_init(&c.s_full[i], 1);
+            mbar_init(&c.s_free[i], 1);
+            mbar_init(&c.p_full[i], kConsumerWarps);
+        }
+        mbar_init(c.cexit, kConsumerWarps + 1);
+        mbar_init(c.drain, 1);
         *c.abort = 0;
         mbar_init_fence();
     }
+    if (warp == 0) tmem_alloc(c.tmem_slot, kTmemCols);
+    tc_fence_before();
     __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp == kConsumerWarps)
-        loader<D>(p, c, lane);
-    else if (warp == kConsumerWarps + 1)
+    tc_fence_after();
+    const uint32_t tbase = *c.tmem_slot;
+    if (warp < kConsumerWarps) {
+        consumer<D>(p, c, warp, lane, tbase);
+    } else if (warp < kConsumerWarps + kLoaderWarps) {
+        loader<D>(p, c, lane, warp - kConsumerWarps);
+    } else if (warp == kConsumerWarps + kLoaderWarps) {
         resolver(p, c, lane);
-    else
-        consumer<D, GMAX>(p, c, warp, lane);
+    } else {
+        if (lane == 0) {
+            mma_issuer<D>(p, c, tbase);
+            tc_fence_before();
+            mbar_arrive(c.cexit);
+        }
+        __syncwarp();
+    }
+    if (warp == 0) {  // the consumers and the MMA thread are done with the tensor memory (bounded wait), then free it
+        drain_wait(c.cexit, 0);
+        tc_fence_after();
+        tmem_dealloc(tbase, kTmemCols);
+    }
 }
 
 // ============================================================== merge of partials
 
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 128;
+constexpr int kMergeBatch = 8;   // records whose loads are in flight together
 
-// For every listed (request, KV head): combine its partial rows.  Draft units
-// have nsplit items x 4 warp records of G rows; split verify units have
-// nsplit records of M rows.  Four output dimensions per thread.
+// For every listed (request, KV head): combine its partial rows.  A split
+// unit has nsplit records of rec_rows rows (M for verify, G for draft).  Each
+// thread owns four output dimensions of one row and merges the records in
+// batches (all loads of a batch in flight), carrying a running max and sums
+// between batches.
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p) {
     const int nm = p.hdr->num_merge;
@@ -807,33 +898,46 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p
         const ReqInfo ri = p.req[b];
         const UnitInfo ui = p.unit[u];
         const bool verify = ri.mode == 1;
-        const int nrows = verify ? p.M : p.G;
-        const int nrec = verify ? ui.nsplit : ui.nsplit * kConsumerWarps;
+        const int nrows = ui.rec_rows, nrec = ui.nsplit;
         for (int idx = threadIdx.x; idx < nrows * (D / 4); idx += kMergeThreads) {
             const int row = idx / (D / 4), c4 = idx - row * (D / 4);
-            float mx = neg_inf();
-            for (int r = 0; r < nrec; ++r) {
-                const size_t pr = verify ? (size_t)ui.rec_base + (size_t)r * p.M + row
-                                         : (size_t)ui.rec_base + (size_t)(r / kConsumerWarps) * ui.rec_rows +
-                                               (size_t)(r % kConsumerWarps) * p.G + row;
-                mx = fmaxf(mx, p.part_lse[pr]);
-            }
+            float mx = neg_inf(), den = 0.f;
             float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-            float lse = neg_inf();
-            if (mx != neg_inf()) {
-                float den = 0.f;
-                for (int r = 0; r < nrec; ++r) {
-                    const size_t pr = verify ? (size_t)ui.rec_base + (size_t)r * p.M + row
-                                             : (size_t)ui.rec_base + (size_t)(r / kConsumerWarps) * ui.rec_rows +
-                                                   (size_t)(r % kConsumerWarps) * p.G + row;
-                    const float w = expf(p.part_lse[pr] - mx);
-                    const float4 v = *reinterpret_cast<const float4 *>(p.part_o + pr * D + 4 * c4);
-                    den += w;
-                    o.x += w * v.x;
-                    o.y += w * v.y;
-                    o.z += w * v.z;
-                    o.w += w * v.w;
+            for (int r0 = 0; r0 < nrec; r0 += kMergeBatch) {
+                float ls[kMergeBatch];
+                float4 v[kMergeBatch];
+#pragma unroll
+                for (int q = 0; q < kMergeBatch; ++q) {
+                    const int r = r0 + q;
+                    if (r < nrec) {
+                        const size_t pr = (size_t)ui.rec_base + (size_t)r * nrows + row;
+                        ls[q] = __ldcg(p.part_lse + pr);
+                        v[q] = __ldcg(reinterpret_cast<const float4 *>(p.part_o + pr * D) + c4);
+                    } else {
+                        ls[q] = neg_inf();
+                        v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                 }
+                float bm = mx;
+#pragma unroll
+                for (int q = 0; q < kMergeBatch; ++q) bm = fmaxf(bm, ls[q]);
+                if (bm == neg_inf()) continue;
+                const float a = expf(mx - bm);  // rescale what was merged so far (0 when empty)
+                den *= a;
+                o = make_float4(o.x * a, o.y * a, o.z * a, o.w * a);
+#pragma unroll
+                for (int q = 0; q < kMergeBatch; ++q) {
+                    const float w = expf(ls[q] - bm);
+                    den += w;
+                    o.x += w * v[q].x;
+                    o.y += w * v[q].y;
+                    o.z += w * v[q].z;
+                    o.w += w * v[q].w;
+                }
+                mx = bm;
+            }
+            float lse = neg_inf();
+            if (den > 0.f) {
                 const float inv = 1.f / den;
                 o = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
                 lse = mx + logf(den);
@@ -855,34 +959,68 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p
 
 // ------------------------------------------------------------------ host-side launch helpers
 
-template <int D, int GMAX>
+template <int D>
 cudaError_t launch_unified_t(const AttnParams &p, int nsm, cudaStream_t st) {
     static int configured_mask = 0;  // one bit per device (up to 32)
-    static int blocks_per_sm[32];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const int bit = 1 << (dev & 31);
     if (!(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & bit)) {
-        e = cudaFuncSetAttribute(unified_attn_kernel<D, GMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Smem<D>::total);
+        e = cudaFuncSetAttribute(unified_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<D>::total);
         if (e != cudaSuccess) return e;
         int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, unified_attn_kernel<D, GMAX>, kThreads,
-                                                          Smem<D>::total);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, unified_attn_kernel<D>, kThreads, Smem<D>::total);
         if (e != cudaSuccess) return e;
-        blocks_per_sm[dev & 31] = n > 0 ? n : 1;
+        // exactly one CTA per SM: it allocates all of the SM's tensor memory
+        if (n != 1) return cudaErrorInvalidConfiguration;
         __atomic_fetch_or(&configured_mask, bit, __ATOMIC_RELEASE);
     }
-    unified_attn_kernel<D, GMAX><<<nsm * blocks_per_sm[dev & 31], kThreads, Smem<D>::total, st>>>(p);
+    unified_attn_kernel<D><<<nsm, kThreads, Smem<D>::total, st>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    merge_kernel<D><<<nsm * 4, kMergeThreads, 0, st>>>(p);
+    merge_kernel<D><<<nsm * 8, kMergeThreads, 0, st>>>(p);
     return cudaGetLastError();
+}
+
+// The tensor-map encoder of the driver, resolved once through the runtime
+// (no link-time dependency on the driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return (EncodeTiledFn) nullptr;
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// A pool [num_slots, Hkv, D] bf16 as the 2-D tensor [num_slots * Hkv rows, D]:
+// boxes of 64 columns x 1 row (the gather4 shape), 128-byte swizzle.
+static cudaError_t pool_tensor_map(CUtensorMap *m, const void *pool, long long num_slots, int Hkv, int D) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t gdim[2] = {(cuuint64_t)D, (cuuint64_t)num_slots * (cuuint64_t)Hkv};
+    const cuuint64_t gstride[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, 1}, estride[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), gdim, gstride, box, estride,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn(const AttnArgs &a, int nsm, cudaStream_t st) {
     AttnParams p;
+    cudaError_t e = pool_tensor_map(&p.tmap_k, a.k_pool, a.num_slots, a.Hkv, a.D);
+    if (e != cudaSuccess) return e;
+    e = pool_tensor_map(&p.tmap_v, a.v_pool, a.num_slots, a.Hkv, a.D);
+    if (e != cudaSuccess) return e;
     p.q = a.q;
     p.k_pool = a.k_pool;
     p.v_pool = a.v_pool;
@@ -906,11 +1044,11 @@ cudaError_t launch_attn(const AttnArgs &a, int nsm, cudaStream_t st) {
     p.G = a.Hq / a.Hkv;
     p.k = a.k;
     p.M = (a.k + 1) * p.G;
+    p.RQ = (p.M + kConsumerWarps - 1) / kConsumerWarps;
+    p.RQd = (p.G + kConsumerWarps - 1) / kConsumerWarps;
     p.max_sparse = a.max_sparse;
     p.scale = a.scale;
-    const bool small_g = p.G <= 4;
-    if (a.D == 128) return small_g ? launch_unified_t<128, 4>(p, nsm, st) : launch_unified_t<128, 8>(p, nsm, st);
-    return small_g ? launch_unified_t<64, 4>(p, nsm, st) : launch_unified_t<64, 8>(p, nsm, st);
+    return a.D == 128 ? launch_unified_t<128>(p, nsm, st) : launch_unified_t<64>(p, nsm, st);
 }
 
 }  // namespace pillar

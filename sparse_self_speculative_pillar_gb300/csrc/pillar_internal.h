@@ -11,8 +11,9 @@
 namespace pillar {
 
 constexpr int kTileKeys = 64;          // keys staged per pipeline stage
-constexpr int kConsumerWarps = 4;      // compute warps per CTA
-constexpr int kThreads = (kConsumerWarps + 2) * 32;  // + a loader warp and a resolver warp
+constexpr int kConsumerWarps = 4;      // compute warps per CTA (one per TMEM lane quadrant)
+constexpr int kLoaderWarps = 4;        // gather warps per CTA (each fetches 64 / kLoaderWarps rows of a tile)
+constexpr int kThreads = (kConsumerWarps + kLoaderWarps + 2) * 32;  // + a resolver and an MMA-issuing warp
 constexpr int kMaxRows = 64;           // (k+1)*G bound of a verify tile
 constexpr int kMaxG = 8;               // query heads per KV head
 constexpr int kDefaultVerifyChunk = 1024;
@@ -33,7 +34,7 @@ struct UnitInfo {
     int nsplit;     // work items of this (request, KV head)
     int item_base;  // index of its first item
     int rec_base;   // first partial row of its items (see AttnLayout)
-    int rec_rows;   // partial rows written per item: 4*G (draft), M (split verify) or 0
+    int rec_rows;   // partial rows written per item of a split unit: M (verify), G (draft); 0 if not split
 };
 
 struct Item {
@@ -63,9 +64,9 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline int verify_chunk_of(const pillar_shape_t &s) { return s.verify_chunk > 0 ? s.verify_chunk : kDefaultVerifyChunk; }
 inline int draft_chunk_of(const pillar_shape_t &s) { return s.draft_chunk > 0 ? s.draft_chunk : kDefaultDraftChunk; }
 
-// Partials: a draft item writes one record per consumer warp (4*G rows), a
-// verify item split over several items writes its M = (k+1)*G rows; each
-// partial row is D fp32 values (the normalised output) plus one fp32 LSE.
+// Partials: an item of a (request, KV head) split over several items writes
+// its rows (M = (k+1)*G for verify, G for draft); each partial row is D fp32
+// values (the normalised output) plus one fp32 LSE.
 inline AttnLayout attn_layout(const pillar_shape_t &s) {
     AttnLayout l{};
     const long long B = s.B, U = (long long)s.B * s.Hkv;
@@ -76,8 +77,7 @@ inline AttnLayout attn_layout(const pillar_shape_t &s) {
     if (dsplit > per_unit) per_unit = dsplit;
     if (per_unit < 1) per_unit = 1;
     l.max_items = U * per_unit;
-    const long long per_item = (long long)kConsumerWarps * G > (long long)(s.k + 1) * G ? (long long)kConsumerWarps * G
-                                                                                          : (long long)(s.k + 1) * G;
+    const long long per_item = (long long)(s.k + 1) * G;
     l.max_rec_rows = l.max_items * per_item;
     size_t off = sizeof(WsHeader);
     l.req = off;        off = align256(off + sizeof(ReqInfo) * B);

@@ -6,15 +6,17 @@
 // split over their context into near-equal chunks of about verify_chunk keys,
 // draft lists into chunks of about draft_chunk listed keys.  Verify items are
 // listed first (they are the heavy ones), then draft items, so the work queue
-// is consumed roughly heaviest-first.  The draft/verify mix in one batch is
+// is consumed roughly heaviest-first; a verify request's items are listed
+// chunk by chunk with the KV heads innermost, so the CTAs that read the same
+// positions (for different heads) run at the same time.  The draft/verify mix in one batch is
 // the unified batch of "SparseSpec-MLSys26" (Unified batch scheduler + fused
 // attention kernel); splitting long contexts over CTAs and merging the pieces
 // by their LSE is this implementation's own load balancing.
 //
-// The planner also places the partial records: every draft item writes one
-// record of G rows per consumer warp, a verify request split over several
-// items writes M = (k+1)*G rows per item; the units that need combining are
-// listed for the merge kernel.
+// The planner also places the partial records: a (request, KV head) split
+// over several items writes one record per item, M = (k+1)*G rows for a
+// verify request, G rows for a draft token; the units that need combining
+// are listed for the merge kernel.
 #include "pillar_device.cuh"
 
 namespace pillar {
@@ -30,32 +32,49 @@ struct PlanParams {
     int B, Hq, Hkv, k, max_sparse, max_len, vchunk, dchunk;
 };
 
-// Exclusive scan over the CTA (kPlanThreads threads); *total gets the sum.
-__device__ long long block_exclusive_scan(long long v, long long *total) {
-    __shared__ long long warp_sums[kPlanThreads / 32];
+constexpr int kScanN = 8;
+
+// Exclusive scan of kScanN values per thread over the CTA (kPlanThreads
+// threads), all at once; tot[] gets the CTA totals.
+__device__ void block_scan8(long long (&v)[kScanN], long long (&tot)[kScanN]) {
+    __shared__ long long warp_sums[kPlanThreads / 32][kScanN];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    long long x = v;
+    long long x[kScanN];
+#pragma unroll
+    for (int i = 0; i < kScanN; ++i) x[i] = v[i];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        long long y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+#pragma unroll
+        for (int i = 0; i < kScanN; ++i) {
+            const long long y = __shfl_up_sync(0xffffffffu, x[i], o);
+            if (lane >= o) x[i] += y;
+        }
     }
-    if (lane == 31) warp_sums[wid] = x;
+    if (lane == 31) {
+#pragma unroll
+        for (int i = 0; i < kScanN; ++i) warp_sums[wid][i] = x[i];
+    }
     __syncthreads();
     if (wid == 0) {
-        long long s = warp_sums[lane];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            long long y = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += y;
+        for (int i = 0; i < kScanN; ++i) {
+            long long t = warp_sums[lane][i];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long y = __shfl_up_sync(0xffffffffu, t, o);
+                if (lane >= o) t += y;
+            }
+            warp_sums[lane][i] = t;
         }
-        warp_sums[lane] = s;
     }
     __syncthreads();
-    const long long base = wid ? warp_sums[wid - 1] : 0;
-    *total = warp_sums[kPlanThreads / 32 - 1];
+#pragma unroll
+    for (int i = 0; i < kScanN; ++i) {
+        const long long base = wid ? warp_sums[wid - 1][i] : 0;
+        tot[i] = warp_sums[kPlanThreads / 32 - 1][i];
+        v[i] = base + x[i] - v[i];
+    }
     __syncthreads();
-    return base + x - v;
 }
 
 // Near-equal chunking of n keys into pieces of at most `chunk` keys, rounded
@@ -72,7 +91,7 @@ __device__ __forceinline__ int chunking(int n, int chunk, int *ns) {
     return cs;
 }
 
-// Keys, split count and chunk size of unit u (request b = u / Hkv).
+// Keys, split count and chunk size of unit u of a request with record r.
 __device__ __forceinline__ int unit_split(const PlanParams &p, const ReqInfo &r, int u, int *n, int *ns, int *bad) {
     if (r.mode == 1) {
         *n = r.len;
@@ -85,134 +104,111 @@ __device__ __forceinline__ int unit_split(const PlanParams &p, const ReqInfo &r,
     return chunking(c, p.dchunk, ns);
 }
 
+// Request record of request b (validated).
+__device__ __forceinline__ ReqInfo read_request(const PlanParams &p, int b, int *bad, int *len_out) {
+    ReqInfo r;
+    r.q_off = r.vidx = 0;
+    const int mode = p.req_mode[b];
+    int len = p.req_len[b];
+    r.mode = mode;
+    if (mode != 0 && mode != 1) *bad |= PILLAR_FLAG_REQUEST, r.mode = -1;
+    if (len < 0) *bad |= PILLAR_FLAG_REQUEST, len = 0;
+    r.len = len;
+    if (r.len > p.max_len) *bad |= PILLAR_FLAG_REQUEST, r.len = p.max_len;
+    if (r.mode == 1 && len < p.k + 1) *bad |= PILLAR_FLAG_REQUEST;
+    *len_out = len;
+    return r;
+}
+
+// One thread per unit (request, KV head), chunks of kPlanThreads units; the
+// unit with g == 0 also carries its request's counts, so one fused scan per
+// chunk gives every offset.
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     const int tid = threadIdx.x;
     const int G = p.Hq / p.Hkv, M = (p.k + 1) * G;
+    const int U = p.B * p.Hkv;
     if (tid == 0) {
         p.hdr->err = 0;
         p.hdr->item_counter = 0;
     }
     int bad = 0;
-
-    // Requests: query-row, KV, verify-index and logits offsets.
-    long long cq = 0, ckv = 0, cv = 0, clg = 0;
-    for (int base = 0; base < p.B; base += kPlanThreads) {
-        const int b = base + tid;
-        int mode = 0, len = 0;
-        if (b < p.B) {
-            mode = p.req_mode[b];
-            len = p.req_len[b];
-        }
-        int eff_mode = mode, proc_len = len;
-        if (b < p.B) {
-            if (mode != 0 && mode != 1) bad |= PILLAR_FLAG_REQUEST, eff_mode = -1;
-            if (len < 0) bad |= PILLAR_FLAG_REQUEST, proc_len = 0, len = 0;
-            if (proc_len > p.max_len) bad |= PILLAR_FLAG_REQUEST, proc_len = p.max_len;
-            if (eff_mode == 1 && len < p.k + 1) bad |= PILLAR_FLAG_REQUEST;
-        }
-        const long long nq = b < p.B ? (eff_mode == 1 ? p.k + 1 : 1) : 0;
-        const long long kvl = b < p.B ? len : 0;
-        const long long isv = (b < p.B && eff_mode == 1) ? 1 : 0;
-        const long long lg = isv ? (long long)p.Hq * (p.k + 1) * len : 0;
-        long long tq, tkv, tv, tlg;
-        const long long oq = block_exclusive_scan(nq, &tq);
-        const long long okv = block_exclusive_scan(kvl, &tkv);
-        const long long ov = block_exclusive_scan(isv, &tv);
-        const long long olg = block_exclusive_scan(lg, &tlg);
-        if (b < p.B) {
-            ReqInfo r;
-            r.q_off = (int)(cq + oq);
-            r.vidx = (int)(cv + ov);
-            r.len = proc_len;
-            r.mode = eff_mode;
-            p.req[b] = r;
-            p.kv_off[b] = ckv + okv;
-            p.logit_off[b] = clg + olg;
-        }
-        cq += tq;
-        ckv += tkv;
-        cv += tv;
-        clg += tlg;
-    }
-    __syncthreads();
-
-    // Units (request, KV head): item bases (verify units first), partial-row
-    // bases and the merge list.
-    const int U = p.B * p.Hkv;
-    long long c_ver_items = 0;
-    {   // pass 0: verify item bases
-        long long carry = 0;
-        for (int base = 0; base < U; base += kPlanThreads) {
-            const int u = base + tid;
-            long long cnt = 0;
-            int n = 0, ns = 1;
-            bool isv = false;
-            if (u < U) {
-                const ReqInfo r = p.req[u / p.Hkv];
-                unit_split(p, r, u, &n, &ns, &bad);
-                isv = r.mode == 1;
-                cnt = isv ? ns : 0;
-            }
-            long long tot;
-            const long long off = block_exclusive_scan(cnt, &tot);
-            if (u < U && isv) p.unit[u].item_base = (int)(carry + off);
-            carry += tot;
-        }
-        c_ver_items = carry;
-    }
-    long long c_items = c_ver_items, c_rec = 0, c_merge = 0;
-    for (int base = 0; base < U; base += kPlanThreads) {   // pass 1: the rest
+    // running totals: q rows, kv positions, verify requests, logits, verify items, draft items, partial rows, merges
+    long long carry[kScanN] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int base = 0; base < U; base += kPlanThreads) {
         const int u = base + tid;
-        long long dcnt = 0, recs = 0, mflag = 0;
-        int n = 0, ns = 1, rec_rows = 0;
-        bool isv = false;
-        if (u < U) {
-            const ReqInfo r = p.req[u / p.Hkv];
-            int dummy = 0;
-            unit_split(p, r, u, &n, &ns, &dummy);
-            isv = r.mode == 1;
-            dcnt = isv ? 0 : ns;
-            rec_rows = isv ? (ns > 1 ? M : 0) : kConsumerWarps * G;
-            recs = (long long)ns * rec_rows;
-            mflag = rec_rows > 0 ? 1 : 0;
+        const bool live = u < U;
+        const int b = live ? u / p.Hkv : 0, g = live ? u - b * p.Hkv : 0;
+        long long v[kScanN] = {0, 0, 0, 0, 0, 0, 0, 0};
+        ReqInfo r;
+        int len = 0, n = 0, ns = 1, rec_rows = 0;
+        if (live) {
+            int ignored = 0;
+            r = read_request(p, b, g == 0 ? &bad : &ignored, &len);  // request problems are flagged once
+            unit_split(p, r, u, &n, &ns, &bad);
+            rec_rows = ns > 1 ? (r.mode == 1 ? M : G) : 0;
+            if (g == 0) {
+                v[0] = r.mode == 1 ? p.k + 1 : 1;
+                v[1] = len;
+                v[2] = r.mode == 1;
+                v[3] = r.mode == 1 ? (long long)p.Hq * (p.k + 1) * len : 0;
+            }
+            if (r.mode == 1) v[4] = ns; else v[5] = ns;
+            v[6] = (long long)ns * rec_rows;
+            v[7] = rec_rows > 0;
         }
-        long long td, tr, tm;
-        const long long od = block_exclusive_scan(dcnt, &td);
-        const long long orr = block_exclusive_scan(recs, &tr);
-        const long long om = block_exclusive_scan(mflag, &tm);
-        if (u < U) {
+        long long tot[kScanN];
+        block_scan8(v, tot);
+        if (live) {
+            if (g == 0) {
+                r.q_off = (int)(carry[0] + v[0]);
+                r.vidx = (int)(carry[2] + v[2]);
+                p.req[b] = r;
+                p.kv_off[b] = carry[1] + v[1];
+                p.logit_off[b] = carry[3] + v[3];
+            }
             UnitInfo ui;
             ui.nsplit = ns;
-            ui.item_base = isv ? p.unit[u].item_base : (int)(c_items + od);
-            ui.rec_base = (int)(c_rec + orr);
             ui.rec_rows = rec_rows;
+            ui.rec_base = (int)(carry[6] + v[6]);
+            // draft bases are relative here; the verify total is added below
+            ui.item_base = (int)(r.mode == 1 ? carry[4] + v[4] : carry[5] + v[5]);
             p.unit[u] = ui;
-            if (mflag) p.merge_list[c_merge + om] = u;
+            if (rec_rows > 0) p.merge_list[carry[7] + v[7]] = u;
         }
-        c_items += td;
-        c_rec += tr;
-        c_merge += tm;
+#pragma unroll
+        for (int i = 0; i < kScanN; ++i) carry[i] += tot[i];
     }
+    const long long ver_items = carry[4];
     if (tid == 0) {
-        p.hdr->num_items = (int)c_items;
+        p.hdr->num_items = (int)(carry[4] + carry[5]);
         p.hdr->num_units = U;
-        p.hdr->num_merge = (int)c_merge;
+        p.hdr->num_merge = (int)carry[7];
     }
-    __syncthreads();
-
-    // Emit the items.
+    // Emit the items (each thread re-reads only the unit it wrote itself).
     for (int u = tid; u < U; u += kPlanThreads) {
-        const ReqInfo r = p.req[u / p.Hkv];
-        const UnitInfo ui = p.unit[u];
-        int n, ns, dummy = 0;
+        const int b = u / p.Hkv;
+        int len, dummy = 0;
+        const ReqInfo r = read_request(p, b, &dummy, &len);
+        UnitInfo ui = p.unit[u];
+        if (r.mode != 1) {
+            ui.item_base += (int)ver_items;
+            p.unit[u].item_base = ui.item_base;
+        }
+        int n, ns;
         const int cs = unit_split(p, r, u, &n, &ns, &dummy);
+        // A verify request's Hkv units all have ns items; they are listed chunk
+        // by chunk, head-minor (request, chunk, head), so the Hkv items reading
+        // the same positions are taken up together.  Draft items stay per unit.
+        const int g = u - b * p.Hkv;
+        const int first = r.mode == 1 ? ui.item_base - g * ns + g : ui.item_base;
+        const int step = r.mode == 1 ? p.Hkv : 1;
         for (int s = 0; s < ns; ++s) {
             Item it;
             it.unit = u;
             it.begin = s * cs;
             it.end = min(n, (s + 1) * cs);
             it.split = s;
-            p.items[ui.item_base + s] = it;
+            p.items[first + s * step] = it;
         }
     }
     if (bad) atomicOr(&p.hdr->err, bad);

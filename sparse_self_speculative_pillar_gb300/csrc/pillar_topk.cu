@@ -32,10 +32,12 @@ struct TopkParams {
 };
 
 constexpr int kScoreThreads = 256;
-constexpr int kScorePerThread = 8;
+constexpr int kScorePerThread = 4;
+constexpr int kScoreRowBatch = 8;  // logit rows whose loads are in flight together
 constexpr int kScoreChunk = kScoreThreads * kScorePerThread;
 constexpr int kSelectThreads = 1024;
-constexpr int kSelectSmemKeys = 48 * 1024;  // keys kept in shared memory (192 KB); longer rows stay in global
+constexpr int kSelectSmemKeys = 40 * 1024;  // keys kept in shared memory (160 KB); longer rows stay in global
+constexpr int kSelectWarps = kSelectThreads / 32;
 
 // Offsets of verify request v in the packed logits (sums over v' < v of
 // Hq*(k+1)*L_v') and in the scores scratch (sums of Hkv*min(L_v', max_len),
@@ -83,26 +85,33 @@ __global__ void __launch_bounds__(kScoreThreads) topk_scores_kernel(const TopkPa
     verify_offsets(p, v, &lg_off, &sc_off);
     const int R = p.row_hi - p.row_lo, nrows = R * p.G;
     __shared__ float s_lse[kMaxRows];
+    __shared__ long long s_row[kMaxRows];
     for (int i = threadIdx.x; i < nrows; i += blockDim.x) {
         const int h = g * p.G + i / R, r = p.row_lo + i % R;
         s_lse[i] = p.lse[((long long)v * p.Hq + h) * (p.k + 1) + r];
+        s_row[i] = lg_off + ((long long)h * (p.k + 1) + r) * L;
     }
     __syncthreads();
     float acc[kScorePerThread];
 #pragma unroll
     for (int e = 0; e < kScorePerThread; ++e) acc[e] = 0.f;
-    for (int i = 0; i < nrows; ++i) {
-        const int h = g * p.G + i / R, r = p.row_lo + i % R;
-        const float *row = p.logits + lg_off + ((long long)h * (p.k + 1) + r) * L;
-        const float ls = s_lse[i];
-        float x[kScorePerThread];
+    for (int i0 = 0; i0 < nrows; i0 += kScoreRowBatch) {
+        float x[kScoreRowBatch][kScorePerThread];
 #pragma unroll
-        for (int e = 0; e < kScorePerThread; ++e) {
-            const int t = t0 + e * kScoreThreads + threadIdx.x;
-            x[e] = t < L ? __ldcs(row + t) : neg_inf();
+        for (int ii = 0; ii < kScoreRowBatch; ++ii) {
+            const int i = i0 + ii;
+#pragma unroll
+            for (int e = 0; e < kScorePerThread; ++e) {
+                const int t = t0 + e * kScoreThreads + threadIdx.x;
+                x[ii][e] = (i < nrows && t < L) ? __ldcs(p.logits + s_row[i] + t) : neg_inf();
+            }
         }
 #pragma unroll
-        for (int e = 0; e < kScorePerThread; ++e) acc[e] += expf(x[e] - ls);
+        for (int ii = 0; ii < kScoreRowBatch; ++ii) {
+            const float ls = i0 + ii < nrows ? s_lse[i0 + ii] : 0.f;
+#pragma unroll
+            for (int e = 0; e < kScorePerThread; ++e) acc[e] += expf(x[ii][e] - ls);
+        }
     }
     const float denom = (float)(R * p.G);
     float *dst = p.scores + sc_off + (long long)g * L;
@@ -145,6 +154,7 @@ __device__ __forceinline__ uint32_t score_key(float s) { return __float_as_uint(
 
 __global__ void __launch_bounds__(kSelectThreads, 1) topk_select_kernel(const TopkParams p) {
     extern __shared__ uint32_t skeys[];
+    __shared__ uint32_t whist[kSelectWarps][256];  // one histogram per warp: no cross-warp atomics
     __shared__ uint32_t hist[256];
     __shared__ uint32_t s_prefix, s_mask, s_remaining;
     const int v = blockIdx.y, g = blockIdx.x, tid = threadIdx.x;
@@ -186,12 +196,20 @@ __global__ void __launch_bounds__(kSelectThreads, 1) topk_select_kernel(const To
     // Radix select, most significant byte first, of the K-th largest key.
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
-        for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
-        __syncthreads();
+        uint32_t *myhist = whist[tid >> 5];
+        for (int i = tid & 31; i < 256; i += 32) myhist[i] = 0;
+        __syncwarp();
         const uint32_t prefix = s_prefix, mask = s_mask;
         for (int t = tid; t < L; t += blockDim.x) {
             const uint32_t key = keys[t] & 0x7fffffffu;
-            if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+            if ((key & mask) == prefix) atomicAdd(&myhist[(key >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (tid < 256) {
+            uint32_t c = 0;
+#pragma unroll 8
+            for (int w = 0; w < kSelectWarps; ++w) c += whist[w][tid];
+            hist[tid] = c;
         }
         __syncthreads();
         if (tid < 32) {
