@@ -457,11 +457,13 @@ __device__ void mma_issuer(const AttnParams &p, const Ctx &c, uint32_t tbase) {
                     if (valid) {
                         const uint32_t sk = smem_u32(c.smem + S::off_stage + stage * S::STAGE);
                         const uint32_t sq = sq0 + qb * S::QHALF;
+                        // descriptors advance by start address (16-byte units): Q 256 B per K step,
+                        // K 32 B per K step inside a 64-column half of 8 KB
+                        const uint64_t da = umma_sdesc(sq, 128, S::CORE_SBO), db = umma_sdesc_sw128(sk, 16, 1024);
 #pragma unroll
-                        for (int ks = 0; ks < D / 16; ++ks)  // K: 64-column halves of 8 KB, 32 bytes per K step
-                            umma_bf16(tbase + sb * kTileKeys, umma_sdesc(sq + ks * 256, 128, S::CORE_SBO),
-                                      umma_sdesc_sw128(sk + (ks >> 2) * (kTileKeys * 128) + (ks & 3) * 32, 16, 1024), idS,
-                                      ks > 0 ? 1u : 0u);
+                        for (int ks = 0; ks < D / 16; ++ks)
+                            umma_bf16(tbase + sb * kTileKeys, da + (uint64_t)(ks * 16),
+                                      db + (uint64_t)((ks >> 2) * (kTileKeys * 8) + (ks & 3) * 2), idS, ks > 0 ? 1u : 0u);
                     }
                     umma_commit(&c.s_full[sb]);
                     if (flags & kLast) {  // the item's query rows are free once its last S has completed
@@ -492,10 +494,10 @@ __device__ void mma_issuer(const AttnParams &p, const Ctx &c, uint32_t tbase) {
                 if (e_valid) {
                     const uint32_t sv = smem_u32(c.smem + S::off_stage + e_stage * S::STAGE + S::ROWS);
                     const uint32_t tO = tbase + S::tO + (uint32_t)e_qb * D;
+                    const uint64_t dv = umma_sdesc_sw128(sv, kTileKeys * 128, 1024);
 #pragma unroll
-                    for (int ks = 0; ks < kTileKeys / 16; ++ks)
-                        umma_bf16_ts(tO, tbase + sb * kTileKeys + ks * 8,  // V: 16 keys = two 8-key atoms
-                                     umma_sdesc_sw128(sv + ks * 2048, kTileKeys * 128, 1024), idO,
+                    for (int ks = 0; ks < kTileKeys / 16; ++ks)  // V: 16 keys = two 8-key atoms = 2048 B
+                        umma_bf16_ts(tO, tbase + sb * kTileKeys + ks * 8, dv + (uint64_t)(ks * 128), idO,
                                      (started || ks > 0) ? 1u : 0u);
                     started = true;
                 }
@@ -770,21 +772,12 @@ __device__ bool attn_item(const AttnParams &p, const Ctx &c, int warp, int lane,
         cur = c.meta[cs.stage];
     }
 
-    // epilogue: the item's last P V has completed
-    if (!mbar_wait(&c.s_free[last_vt % kSBuf], (last_vt / kSBuf) & 1, c.abort, c.err)) return false;
-    tc_fence_after();
+    // epilogue: row sums and LSEs first, then the O rows once the item's last P V has completed
     ra.l += __shfl_xor_sync(0xffffffffu, ra.l, 1);
     ra.l += __shfl_xor_sync(0xffffffffu, ra.l, 2);
     rb.l += __shfl_xor_sync(0xffffffffu, rb.l, 1);
     rb.l += __shfl_xor_sync(0xffffffffu, rb.l, 2);
     const float inva = ra.l > 0.f ? 1.f / ra.l : 0.f, invb = rb.l > 0.f ? 1.f / rb.l : 0.f;
-#pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 64) {
-        float ov[32];
-        tmem_ld16x256b_x8(tO + lane_base + c0, ov);  // warp-collective: every lane loads
-        row_output<D, 0>(p, in, ra, ov, c0, cq, inva);
-        if (have_b) row_output<D, 2>(p, in, rb, ov, c0, cq, invb);
-    }
     if ((lane & 3) == 0 && (verify || in.nsplit > 1)) {
         const int kk1 = p.k + 1;
 #pragma unroll
@@ -797,6 +790,15 @@ __device__ bool attn_item(const AttnParams &p, const Ctx &c, int warp, int lane,
             else
                 p.part_lse[(size_t)in.rec + r.row] = lse;
         }
+    }
+    if (!mbar_wait(&c.s_free[last_vt % kSBuf], (last_vt / kSBuf) & 1, c.abort, c.err)) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 64) {
+        float ov[32];
+        tmem_ld16x256b_x8(tO + lane_base + c0, ov);  // warp-collective: every lane loads
+        row_output<D, 0>(p, in, ra, ov, c0, cq, inva);
+        if (have_b) row_output<D, 2>(p, in, rb, ov, c0, cq, invb);
     }
     tc_fence_before();
     __syncwarp();
@@ -884,76 +886,81 @@ __global__ void __launch_bounds__(kThreads, 1) unified_attn_kernel(const __grid_
 constexpr int kMergeThreads = 128;
 constexpr int kMergeBatch = 8;   // records whose loads are in flight together
 
-// For every listed (request, KV head): combine its partial rows.  A split
-// unit has nsplit records of rec_rows rows (M for verify, G for draft).  Each
-// thread owns four output dimensions of one row and merges the records in
-// batches (all loads of a batch in flight), carrying a running max and sums
-// between batches.
+// Combines the partial rows of every split (request, KV head).  A split unit
+// has nsplit records of rec_rows rows (M for verify, G for draft); the work is
+// flattened over (listed unit, row, four output dimensions), one thread each,
+// so that few, long units still spread over the whole GPU.  A thread merges
+// its records in batches (all loads of a batch in flight), carrying a running
+// max and sums between batches.
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p) {
     const int nm = p.hdr->num_merge;
-    for (int li = blockIdx.x; li < nm; li += gridDim.x) {
+    const int per_unit = p.M * (D / 4);  // thread slots per listed unit (rows up to M)
+    const long long total = (long long)nm * per_unit;
+    for (long long w = (long long)blockIdx.x * kMergeThreads + threadIdx.x; w < total;
+         w += (long long)gridDim.x * kMergeThreads) {
+        const int li = (int)(w / per_unit);
+        const int idx = (int)(w - (long long)li * per_unit);
         const int u = p.merge_list[li];
+        const UnitInfo ui = p.unit[u];
+        const int nrows = ui.rec_rows, nrec = ui.nsplit;
+        const int row = idx / (D / 4), c4 = idx - row * (D / 4);
+        if (row >= nrows) continue;
         const int b = u / p.Hkv, g = u - b * p.Hkv;
         const ReqInfo ri = p.req[b];
-        const UnitInfo ui = p.unit[u];
         const bool verify = ri.mode == 1;
-        const int nrows = ui.rec_rows, nrec = ui.nsplit;
-        for (int idx = threadIdx.x; idx < nrows * (D / 4); idx += kMergeThreads) {
-            const int row = idx / (D / 4), c4 = idx - row * (D / 4);
-            float mx = neg_inf(), den = 0.f;
-            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int r0 = 0; r0 < nrec; r0 += kMergeBatch) {
-                float ls[kMergeBatch];
-                float4 v[kMergeBatch];
+        float mx = neg_inf(), den = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r0 = 0; r0 < nrec; r0 += kMergeBatch) {
+            float ls[kMergeBatch];
+            float4 v[kMergeBatch];
 #pragma unroll
-                for (int q = 0; q < kMergeBatch; ++q) {
-                    const int r = r0 + q;
-                    if (r < nrec) {
-                        const size_t pr = (size_t)ui.rec_base + (size_t)r * nrows + row;
-                        ls[q] = __ldcg(p.part_lse + pr);
-                        v[q] = __ldcg(reinterpret_cast<const float4 *>(p.part_o + pr * D) + c4);
-                    } else {
-                        ls[q] = neg_inf();
-                        v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
+            for (int q = 0; q < kMergeBatch; ++q) {
+                const int r = r0 + q;
+                if (r < nrec) {
+                    const size_t pr = (size_t)ui.rec_base + (size_t)r * nrows + row;
+                    ls[q] = __ldcg(p.part_lse + pr);
+                    v[q] = __ldcg(reinterpret_cast<const float4 *>(p.part_o + pr * D) + c4);
+                } else {
+                    ls[q] = neg_inf();
+                    v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                float bm = mx;
+            }
+            float bm = mx;
 #pragma unroll
-                for (int q = 0; q < kMergeBatch; ++q) bm = fmaxf(bm, ls[q]);
-                if (bm == neg_inf()) continue;
-                const float a = expf(mx - bm);  // rescale what was merged so far (0 when empty)
-                den *= a;
-                o = make_float4(o.x * a, o.y * a, o.z * a, o.w * a);
+            for (int q = 0; q < kMergeBatch; ++q) bm = fmaxf(bm, ls[q]);
+            if (bm == neg_inf()) continue;
+            const float a = expf(mx - bm);  // rescale what was merged so far (0 when empty)
+            den *= a;
+            o = make_float4(o.x * a, o.y * a, o.z * a, o.w * a);
 #pragma unroll
-                for (int q = 0; q < kMergeBatch; ++q) {
-                    const float w = expf(ls[q] - bm);
-                    den += w;
-                    o.x += w * v[q].x;
-                    o.y += w * v[q].y;
-                    o.z += w * v[q].z;
-                    o.w += w * v[q].w;
-                }
-                mx = bm;
+            for (int q = 0; q < kMergeBatch; ++q) {
+                const float wq = expf(ls[q] - bm);
+                den += wq;
+                o.x += wq * v[q].x;
+                o.y += wq * v[q].y;
+                o.z += wq * v[q].z;
+                o.w += wq * v[q].w;
             }
-            float lse = neg_inf();
-            if (den > 0.f) {
-                const float inv = 1.f / den;
-                o = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
-                lse = mx + logf(den);
-            }
-            int j = 0, gi = row;
-            if (verify) {
-                j = row / p.G;
-                gi = row - j * p.G;
-            }
-            const size_t orow = (size_t)(ri.q_off + j) * p.Hq + (size_t)g * p.G + gi;
-            uint2 pk;
-            pk.x = pack_bf16x2(o.x, o.y);
-            pk.y = pack_bf16x2(o.z, o.w);
-            *reinterpret_cast<uint2 *>(p.out + orow * D + 4 * c4) = pk;
-            if (verify && c4 == 0) p.lse[((size_t)ri.vidx * p.Hq + (size_t)g * p.G + gi) * (p.k + 1) + j] = lse;
+            mx = bm;
         }
+        float lse = neg_inf();
+        if (den > 0.f) {
+            const float inv = 1.f / den;
+            o = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+            lse = mx + logf(den);
+        }
+        int j = 0, gi = row;
+        if (verify) {
+            j = row / p.G;
+            gi = row - j * p.G;
+        }
+        const size_t orow = (size_t)(ri.q_off + j) * p.Hq + (size_t)g * p.G + gi;
+        uint2 pk;
+        pk.x = pack_bf16x2(o.x, o.y);
+        pk.y = pack_bf16x2(o.z, o.w);
+        *reinterpret_cast<uint2 *>(p.out + orow * D + 4 * c4) = pk;
+        if (verify && c4 == 0) p.lse[((size_t)ri.vidx * p.Hq + (size_t)g * p.G + gi) * (p.k + 1) + j] = lse;
     }
 }
 
@@ -979,7 +986,7 @@ cudaError_t launch_unified_t(const AttnParams &p, int nsm, cudaStream_t st) {
     unified_attn_kernel<D><<<nsm, kThreads, Smem<D>::total, st>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    merge_kernel<D><<<nsm * 8, kMergeThreads, 0, st>>>(p);
+    merge_kernel<D><<<nsm * 16, kMergeThreads, 0, st>>>(p);
     return cudaGetLastError();
 }
 
