@@ -24,8 +24,7 @@
 //     TMA tile::gather4 (four 256-byte page-size-1 rows per copy) in the
 //     swizzled layout the tensor cores read, completion counted in bytes on
 //     the stage's mbarrier; the item's query rows go to their operand slots
-//     with the first tile and its metadata travels in the stage record.  For
-//     verify items they first prefetch whole slot blocks into L2 (see loader());
+//     with the first tile and its metadata travels in the stage record;
 //   * MMA warp (one thread): issues all tensor-core work -- S = Q K^T
 //     (M = 64 query-row slots, N = 64 keys) into one of four S buffers in
 //     tensor memory as soon as a tile has landed, and O += P V with P read
@@ -281,13 +280,6 @@ __device__ void resolver(const AttnParams &p, const Ctx &c, int lane) {
 // tensor cores read, split in 64-column halves; each announces its bytes on
 // the stage barrier.  All loaders run the same deterministic sequence; loader
 // 0 also stages the query rows (16-byte cp.async) and writes the stage record.
-// At the start of a verify item each loader prefetches into L2 whole slot
-// blocks (all KV heads of a position, Hkv*D*2 contiguous bytes of K and of
-// V) for the positions p = g (mod Hkv): verify items are ordered request,
-// chunk, head, so the Hkv CTAs working on one chunk run side by side and
-// each fetches an Hkv-th of the blocks for all of them.  The pool's 256-byte
-// head rows then come from L2; HBM sees whole-block reads, which it serves
-// far faster than scattered 256-byte ones.
 template <int D>
 __device__ void loader(const AttnParams &p, const Ctx &c, int lane, int li) {
     using S = Smem<D>;
@@ -298,9 +290,6 @@ __device__ void loader(const AttnParams &p, const Ctx &c, int lane, int li) {
     int stage = 0, qn = 0;
     uint32_t phase = 0, qph = 0, fph = 0, issued = 0, issued_par = 0;
     bool ok = true;
-    const char *kpool = reinterpret_cast<const char *>(p.k_pool);
-    const char *vpool = reinterpret_cast<const char *>(p.v_pool);
-    const uint32_t block_bytes = (uint32_t)p.Hkv * D * 2;
     // this lane's gather4: row group rgl of the warp's rows, K (kv 0) or V (kv 1), column half h
     const int rgl = lane % GW, kv = (lane / GW) & 1, h = lane / (2 * GW);
     const bool gl = h < NH;
@@ -327,16 +316,6 @@ __device__ void loader(const AttnParams &p, const Ctx &c, int lane, int li) {
         const int ntiles = n > 0 ? (n + kTileKeys - 1) / kTileKeys : 1;
         const int qb = qn & 1;  // two query buffers: this item's may still hold the one before last
         ++qn;
-        if (verify) {  // this CTA's share of the chunk's slot blocks, into L2
-            const int i0 = ((g - info.begin) % p.Hkv + p.Hkv) % p.Hkv;
-            for (int i = i0 + p.Hkv * (li * 32 + lane); i < n; i += p.Hkv * 32 * kLoaderWarps) {
-                const int sl = rows[i];
-                if (sl >= 0) {
-                    bulk_prefetch_l2(kpool + (size_t)sl * block_bytes, block_bytes);
-                    bulk_prefetch_l2(vpool + (size_t)sl * block_bytes, block_bytes);
-                }
-            }
-        }
         for (int t = 0; t < ntiles; ++t) {
             ok = mbar_wait(&c.empty[stage], phase ^ 1, c.abort, c.err);
             if (!ok) break;

@@ -8,7 +8,8 @@
 // listed first (they are the heavy ones), then draft items, so the work queue
 // is consumed roughly heaviest-first; a verify request's items are listed
 // chunk by chunk with the KV heads innermost, so the CTAs that read the same
-// positions (for different heads) run at the same time.  The draft/verify mix in one batch is
+// positions (neighbouring 256-byte rows of the same slot blocks, one per
+// head) run at the same time.  The draft/verify mix in one batch is
 // the unified batch of "SparseSpec-MLSys26" (Unified batch scheduler + fused
 // attention kernel); splitting long contexts over CTAs and merging the pieces
 // by their LSE is this implementation's own load balancing.
