@@ -839,6 +839,9 @@ __global__ void __launch_bounds__(kThreads, 1) unified_attn_kernel(const __grid_
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *c.tmem_slot;
+    // Everything above is private to the CTA; the plan's output is read only from here on.
+    pdl_wait_prerequisites();
+    pdl_launch_dependents();  // the merge kernel waits for this kernel's completion itself
     if (warp < kConsumerWarps) {
         consumer<D>(p, c, warp, lane, tbase);
     } else if (warp < kConsumerWarps + kLoaderWarps) {
@@ -873,6 +876,7 @@ constexpr int kMergeBatch = 8;   // records whose loads are in flight together
 // max and sums between batches.
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p) {
+    pdl_wait_prerequisites();  // the partials come from the attention kernel
     const int nm = p.hdr->num_merge;
     const int per_unit = p.M * (D / 4);  // thread slots per listed unit (rows up to M)
     const long long total = (long long)nm * per_unit;
@@ -962,11 +966,24 @@ cudaError_t launch_unified_t(const AttnParams &p, int nsm, cudaStream_t st) {
         if (n != 1) return cudaErrorInvalidConfiguration;
         __atomic_fetch_or(&configured_mask, bit, __ATOMIC_RELEASE);
     }
-    unified_attn_kernel<D><<<nsm, kThreads, Smem<D>::total, st>>>(p);
-    e = cudaGetLastError();
+    // Both kernels are launched as programmatic dependents of the one before
+    // them on the stream: their launch and prologue overlap its tail.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nsm);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Smem<D>::total;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, unified_attn_kernel<D>, p);
     if (e != cudaSuccess) return e;
-    merge_kernel<D><<<nsm * 16, kMergeThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    cfg.gridDim = dim3(nsm * 16);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, merge_kernel<D>, p);
 }
 
 // The tensor-map encoder of the driver, resolved once through the runtime

@@ -20,6 +20,16 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
     return t;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Lets the next kernel on the stream (launched with programmatic stream
+// serialization) start its prologue before this one finishes.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Blocks until the kernels this one depends on have completed and their
+// memory is visible (a no-op when it was launched without the attribute).
+__device__ __forceinline__ void pdl_wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {

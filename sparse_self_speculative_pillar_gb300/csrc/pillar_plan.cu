@@ -125,6 +125,9 @@ __device__ __forceinline__ ReqInfo read_request(const PlanParams &p, int b, int 
 // unit with g == 0 also carries its request's counts, so one fused scan per
 // chunk gives every offset.
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
+    // the attention kernel may start its prologue (barriers, tensor memory) now;
+    // it reads nothing of this kernel's output before this kernel completes
+    pdl_launch_dependents();
     const int tid = threadIdx.x;
     const int G = p.Hq / p.Hkv, M = (p.k + 1) * G;
     const int U = p.B * p.Hkv;

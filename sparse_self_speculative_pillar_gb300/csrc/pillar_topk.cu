@@ -32,7 +32,7 @@ struct TopkParams {
 };
 
 constexpr int kScoreThreads = 256;
-constexpr int kScorePerThread = 4;
+constexpr int kScorePerThread = 2;
 constexpr int kScoreRowBatch = 8;  // logit rows whose loads are in flight together
 constexpr int kScoreChunk = kScoreThreads * kScorePerThread;
 constexpr int kSelectThreads = 1024;
