@@ -566,10 +566,13 @@ __device__ __forceinline__ float row_scores(const AttnParams &p, const StageMeta
     if (!r.act) return neg_inf();
     const bool interior = cur.nk == kTileKeys && cur.valid == ~0ull && cur.pos0 + kTileKeys - 1 <= r.lim;
     if (interior) {
+        const float2 sc = make_float2(p.scale, p.scale);
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) s[4 * c + OFF + e] *= p.scale;
+        for (int c = 0; c < 8; ++c) {  // packed pairs: one fp32x2 multiply per two scores
+            const float2 v = fmul2(make_float2(s[4 * c + OFF], s[4 * c + OFF + 1]), sc);
+            s[4 * c + OFF] = v.x;
+            s[4 * c + OFF + 1] = v.y;
+        }
     } else {
 #pragma unroll
         for (int c = 0; c < 8; ++c)
@@ -619,19 +622,17 @@ template <int OFF>
 __device__ __forceinline__ void row_probs(VRow &r, const float *s, uint32_t *pw) {
     if (r.act) {
         const float nb = -(r.m == neg_inf() ? 0.f : r.m) * kLog2e;
-        float l8[8];
+        const float2 k2 = make_float2(kLog2e, kLog2e), b2 = make_float2(nb, nb);
+        float2 l4[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const float p0 = ex2_approx(fmaf(s[4 * c + OFF], kLog2e, nb));
-            const float p1 = ex2_approx(fmaf(s[4 * c + OFF + 1], kLog2e, nb));
-            l8[c] = p0 + p1;
-            pw[2 * c + OFF / 2] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < 8; ++c) {  // packed pairs: exponent arguments and sums two at a time
+            const float2 a = ffma2(make_float2(s[4 * c + OFF], s[4 * c + OFF + 1]), k2, b2);
+            const float2 pe = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+            l4[c & 3] = c < 4 ? pe : fadd2(l4[c & 3], pe);
+            pw[2 * c + OFF / 2] = pack_bf16x2(pe.x, pe.y);
         }
-#pragma unroll
-        for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-            for (int c = 0; c < w; ++c) l8[c] += l8[c + w];
-        r.l += l8[0];
+        const float2 l2 = fadd2(fadd2(l4[0], l4[1]), fadd2(l4[2], l4[3]));
+        r.l += l2.x + l2.y;
     } else {
 #pragma unroll
         for (int c = 0; c < 8; ++c) pw[2 * c + OFF / 2] = 0u;

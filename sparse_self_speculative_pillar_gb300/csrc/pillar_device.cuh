@@ -322,6 +322,23 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 d) {
     return *reinterpret_cast<float2 *>(&ud);
 }
 
+// Packed fp32 pair multiply and add (sm_100+).
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    unsigned long long ua = *reinterpret_cast<unsigned long long *>(&a);
+    unsigned long long ub = *reinterpret_cast<unsigned long long *>(&b);
+    unsigned long long ud;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(ud) : "l"(ua), "l"(ub));
+    return *reinterpret_cast<float2 *>(&ud);
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    unsigned long long ua = *reinterpret_cast<unsigned long long *>(&a);
+    unsigned long long ub = *reinterpret_cast<unsigned long long *>(&b);
+    unsigned long long ud;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(ud) : "l"(ua), "l"(ub));
+    return *reinterpret_cast<float2 *>(&ud);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
