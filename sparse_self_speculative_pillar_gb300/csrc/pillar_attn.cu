@@ -278,8 +278,9 @@ __device__ void resolver(const AttnParams &p, const Ctx &c, int lane) {
 // RW = 64 / kLoaderWarps, of K and of V by TMA tile::gather4 (four rows per
 // copy, each lane issuing its own) into the 128-byte-swizzled layout the
 // tensor cores read, split in 64-column halves; each announces its bytes on
-// the stage barrier.  All loaders run the same deterministic sequence; loader
-// 0 also stages the query rows (16-byte cp.async) and writes the stage record.
+// the stage barrier.  All loaders run the same deterministic sequence and
+// share the query rows of an item's first tile (16-byte cp.async); loader 0
+// writes the stage record.
 template <int D>
 __device__ void loader(const AttnParams &p, const Ctx &c, int lane, int li) {
     using S = Smem<D>;
@@ -301,7 +302,7 @@ __device__ void loader(const AttnParams &p, const Ctx &c, int lane, int li) {
         if (info.it < 0) {
             ok = mbar_wait(&c.empty[stage], phase ^ 1, c.abort, c.err);
             if (ok) {
-                if (li == 0) cp_async_arrive_noinc(&c.full[stage]);
+                cp_async_arrive_noinc(&c.full[stage]);
                 __syncwarp();
                 if (lane == 0) {
                     if (li == 0) c.meta[stage].flags = kStop;
@@ -319,7 +320,7 @@ __device__ void loader(const AttnParams &p, const Ctx &c, int lane, int li) {
         for (int t = 0; t < ntiles; ++t) {
             ok = mbar_wait(&c.empty[stage], phase ^ 1, c.abort, c.err);
             if (!ok) break;
-            if (t == 0 && li == 0) {
+            if (t == 0) {  // every loader writes query rows: the buffer's previous item must be done with it
                 ok = mbar_wait(&c.qempty[qb], ((qph >> qb) & 1) ^ 1, c.abort, c.err);
                 if (!ok) break;
                 qph ^= 1u << qb;
@@ -365,21 +366,19 @@ __device__ void loader(const AttnParams &p, const Ctx &c, int lane, int li) {
                                 rr[3], &c.full[stage]);
                 }
             }
-            if (li == 0) {
-                if (t == 0) {  // query rows into their operand slots, core-matrix layout
-                    char *qreg = c.smem + S::off_q + qb * S::QHALF;
-                    const int nchunks = (verify ? p.M : p.G) * S::KCH;
-                    const int rq = verify ? p.RQ : p.RQd;
-                    for (int i = lane; i < nchunks; i += 32) {
-                        const int r = i / S::KCH, cc = i - r * S::KCH;
-                        const int j = verify ? r / p.G : 0, gi = r - j * p.G;
-                        const int a = row_slot(r, rq);
-                        cp_async16(qreg + (a >> 3) * S::CORE_SBO + cc * 128 + (a & 7) * 16,
-                                   p.q + ((size_t)(info.q_off + j) * p.Hq + (size_t)g * p.G + gi) * D + cc * 8);
-                    }
+            if (t == 0) {  // query rows into their operand slots (core-matrix layout), shared by the loaders
+                char *qreg = c.smem + S::off_q + qb * S::QHALF;
+                const int nchunks = (verify ? p.M : p.G) * S::KCH;
+                const int rq = verify ? p.RQ : p.RQd;
+                for (int i = li * 32 + lane; i < nchunks; i += 32 * kLoaderWarps) {
+                    const int r = i / S::KCH, cc = i - r * S::KCH;
+                    const int j = verify ? r / p.G : 0, gi = r - j * p.G;
+                    const int a = row_slot(r, rq);
+                    cp_async16(qreg + (a >> 3) * S::CORE_SBO + cc * 128 + (a & 7) * 16,
+                               p.q + ((size_t)(info.q_off + j) * p.Hq + (size_t)g * p.G + gi) * D + cc * 8);
                 }
-                cp_async_arrive_noinc(&c.full[stage]);  // lands with this lane's query copies (if any)
             }
+            cp_async_arrive_noinc(&c.full[stage]);  // lands with this lane's query copies (if any)
             issued |= 1u << stage;
             issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
             if (++stage == S::NSTAGE) {
@@ -696,13 +695,14 @@ __device__ bool attn_item(const AttnParams &p, const Ctx &c, int warp, int lane,
         const float mna = fmaxf(ra.m, mta), mnb = fmaxf(rb.m, mtb);
         const bool grow_a = ra.act && ra.m != neg_inf() && (mna - ra.m) * kLog2e > kRescaleLog2;
         const bool grow_b = rb.act && rb.m != neg_inf() && (mnb - rb.m) * kLog2e > kRescaleLog2;
-        const float aa = grow_a ? exp2f((ra.m - mna) * kLog2e) : 1.f;
-        const float ab = grow_b ? exp2f((rb.m - mnb) * kLog2e) : 1.f;
+        float aa = 1.f, ab = 1.f;  // rescale factors, computed only on the rare growth
         if (grow_a) {
+            aa = exp2f((ra.m - mna) * kLog2e);
             ra.l *= aa;
             ra.m = mna;
         }
         if (grow_b) {
+            ab = exp2f((rb.m - mnb) * kLog2e);
             rb.l *= ab;
             rb.m = mnb;
         }
@@ -814,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1) unified_attn_kernel(const __grid_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S::NSTAGE; ++s) {
-            mbar_init(&c.full[s], kLoaderWarps + 32);  // one byte-count arrival per loader + loader 0's query-copy arrivals
+            mbar_init(&c.full[s], kLoaderWarps * 33);  // per loader: a byte-count arrival + its lanes' query-copy arrivals
             mbar_init(&c.empty[s], kConsumerWarps + 1);    // one per consumer warp + the MMA thread
         }
         for (int i = 0; i < 2; ++i) {
