@@ -18,6 +18,8 @@
 //      of the (non-negative) fp32 score, then an ordered compaction that
 //      keeps everything above the threshold plus the lowest positions equal
 //      to it -- the output comes out ascending with no sort.
+// The two are chained by programmatic dependent launch: the select grid is
+// scheduled while the scores finish and waits for them before reading.
 #include "pillar_device.cuh"
 
 namespace pillar {
@@ -30,6 +32,15 @@ struct TopkParams {
     float *scores;
     int V, Hq, Hkv, G, k, row_lo, row_hi, max_topk, max_len, smem_keys;
 };
+
+// exp(y) as 2^(y log2 e) by the hardware's approximate base-2 exponential,
+// subnormal results kept (relative error ~2^-22; y = logit - lse <= 0, so
+// the difference is formed first and is exact near the row maximum).
+__device__ __forceinline__ float exp2_sub(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 constexpr int kScoreThreads = 256;
 constexpr int kScorePerThread = 2;
@@ -73,6 +84,11 @@ __device__ void verify_offsets(const TopkParams &p, int v, long long *lg_off, lo
 }
 
 __global__ void __launch_bounds__(kScoreThreads) topk_scores_kernel(const TopkParams p) {
+    // The select kernel may be scheduled now; it reads the scores only after
+    // this grid has completed.  Nothing here is read or written before the
+    // kernels ahead on the stream are complete.
+    pdl_launch_dependents();
+    pdl_wait_prerequisites();
     const int v = blockIdx.z, g = blockIdx.y;
     const int L = p.req_len[p.group_map[v]];
     const int t0 = blockIdx.x * kScoreChunk;
@@ -95,22 +111,24 @@ __global__ void __launch_bounds__(kScoreThreads) topk_scores_kernel(const TopkPa
     float acc[kScorePerThread];
 #pragma unroll
     for (int e = 0; e < kScorePerThread; ++e) acc[e] = 0.f;
+    const bool whole = t0 + kScoreChunk <= L;  // no position of this chunk is past the row's end
     for (int i0 = 0; i0 < nrows; i0 += kScoreRowBatch) {
         float x[kScoreRowBatch][kScorePerThread];
 #pragma unroll
         for (int ii = 0; ii < kScoreRowBatch; ++ii) {
             const int i = i0 + ii;
+            const float *row = p.logits + (i < nrows ? s_row[i] : 0ll) + t0 + threadIdx.x;
 #pragma unroll
             for (int e = 0; e < kScorePerThread; ++e) {
-                const int t = t0 + e * kScoreThreads + threadIdx.x;
-                x[ii][e] = (i < nrows && t < L) ? __ldcs(p.logits + s_row[i] + t) : neg_inf();
+                const bool in = i < nrows && (whole || t0 + e * kScoreThreads + (int)threadIdx.x < L);
+                x[ii][e] = in ? __ldcs(row + e * kScoreThreads) : neg_inf();
             }
         }
 #pragma unroll
         for (int ii = 0; ii < kScoreRowBatch; ++ii) {
             const float ls = i0 + ii < nrows ? s_lse[i0 + ii] : 0.f;
 #pragma unroll
-            for (int e = 0; e < kScorePerThread; ++e) acc[e] += expf(x[ii][e] - ls);
+            for (int e = 0; e < kScorePerThread; ++e) acc[e] += exp2_sub((x[ii][e] - ls) * kLog2e);
         }
     }
     const float denom = (float)(R * p.G);
@@ -157,6 +175,7 @@ __global__ void __launch_bounds__(kSelectThreads, 1) topk_select_kernel(const To
     __shared__ uint32_t whist[kSelectWarps][256];  // one histogram per warp: no cross-warp atomics
     __shared__ uint32_t hist[256];
     __shared__ uint32_t s_prefix, s_mask, s_remaining;
+    pdl_wait_prerequisites();  // the scores (and everything before them) are complete and visible
     const int v = blockIdx.y, g = blockIdx.x, tid = threadIdx.x;
     const int L = p.req_len[p.group_map[v]];
     if (L < 0 || L > p.max_len) {
@@ -181,7 +200,20 @@ __global__ void __launch_bounds__(kSelectThreads, 1) topk_select_kernel(const To
     const float *sc = p.scores + sc_off + (long long)g * L;
     const uint32_t *keys;
     if (L <= p.smem_keys) {
-        for (int t = tid; t < L; t += blockDim.x) skeys[t] = score_key(sc[t]);
+        constexpr int kU = 8;  // independent loads in flight per thread
+        for (int t0 = 0; t0 < L; t0 += kU * kSelectThreads) {
+            float x[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int t = t0 + u * kSelectThreads + tid;
+                x[u] = t < L ? sc[t] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int t = t0 + u * kSelectThreads + tid;
+                if (t < L) skeys[t] = score_key(x[u]);
+            }
+        }
         keys = skeys;
     } else {
         keys = reinterpret_cast<const uint32_t *>(sc);  // signless already: scores are >= 0
@@ -308,13 +340,25 @@ cudaError_t launch_topk_select(const TopkArgs &a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         __atomic_fetch_or(&configured_mask, bit, __ATOMIC_RELEASE);
     }
-    dim3 g1((p.max_len + kScoreChunk - 1) / kScoreChunk, p.Hkv, p.V);
-    topk_scores_kernel<<<g1, kScoreThreads, 0, st>>>(p);
-    e = cudaGetLastError();
+    // Both kernels are programmatic dependents of the one before them on the
+    // stream: their launch overlaps its tail, and each waits for it to
+    // complete before touching memory.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.max_len + kScoreChunk - 1) / kScoreChunk, p.Hkv, p.V);
+    cfg.blockDim = dim3(kScoreThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, topk_scores_kernel, p);
     if (e != cudaSuccess) return e;
-    dim3 g2(p.Hkv, p.V);
-    topk_select_kernel<<<g2, kSelectThreads, sel_smem, st>>>(p);
-    return cudaGetLastError();
+    cfg.gridDim = dim3(p.Hkv, p.V);
+    cfg.blockDim = dim3(kSelectThreads);
+    cfg.dynamicSmemBytes = sel_smem;
+    return cudaLaunchKernelEx(&cfg, topk_select_kernel, p);
 }
 
 }  // namespace pillar
