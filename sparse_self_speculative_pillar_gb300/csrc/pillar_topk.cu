@@ -33,15 +33,6 @@ struct TopkParams {
     int V, Hq, Hkv, G, k, row_lo, row_hi, max_topk, max_len, smem_keys;
 };
 
-// exp(y) as 2^(y log2 e) by the hardware's approximate base-2 exponential,
-// subnormal results kept (relative error ~2^-22; y = logit - lse <= 0, so
-// the difference is formed first and is exact near the row maximum).
-__device__ __forceinline__ float exp2_sub(float x) {
-    float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 constexpr int kScoreThreads = 256;
 constexpr int kScorePerThread = 2;
 constexpr int kScoreRowBatch = 8;  // logit rows whose loads are in flight together
@@ -53,34 +44,60 @@ constexpr int kSelectWarps = kSelectThreads / 32;
 // Offsets of verify request v in the packed logits (sums over v' < v of
 // Hq*(k+1)*L_v') and in the scores scratch (sums of Hkv*min(L_v', max_len),
 // so that a bad length can never push a later request past the workspace).
-// Every thread of the block gets them.
+// Warp 0 computes them; every thread of the block gets them.
 __device__ void verify_offsets(const TopkParams &p, int v, long long *lg_off, long long *sc_off) {
-    __shared__ long long red[2][32];
-    long long s = 0, c = 0;
-    for (int i = threadIdx.x; i < v; i += blockDim.x) {
-        const int l = p.req_len[p.group_map[i]];
-        s += l;
-        c += l < 0 ? 0 : (l > p.max_len ? p.max_len : l);
-    }
+    __shared__ long long s_off[2];
+    if (threadIdx.x < 32) {
+        long long s = 0, c = 0;
+        for (int i = threadIdx.x; i < v; i += 32) {
+            const int l = p.req_len[p.group_map[i]];
+            s += l;
+            c += l < 0 ? 0 : (l > p.max_len ? p.max_len : l);
+        }
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        s += __shfl_xor_sync(0xffffffffu, s, o);
-        c += __shfl_xor_sync(0xffffffffu, c, o);
-    }
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    if (lane == 0) {
-        red[0][wid] = s;
-        red[1][wid] = c;
-    }
-    __syncthreads();
-    long long ts = 0, tc = 0;
-    for (int w = 0; w < nw; ++w) {
-        ts += red[0][w];
-        tc += red[1][w];
+        for (int o = 16; o >= 1; o >>= 1) {
+            s += __shfl_xor_sync(0xffffffffu, s, o);
+            c += __shfl_xor_sync(0xffffffffu, c, o);
+        }
+        if (threadIdx.x == 0) {
+            s_off[0] = s * p.Hq * (p.k + 1);
+            s_off[1] = c * p.Hkv;
+        }
     }
     __syncthreads();
-    *lg_off = ts * p.Hq * (p.k + 1);
-    *sc_off = tc * p.Hkv;
+    *lg_off = s_off[0];
+    *sc_off = s_off[1];
+}
+
+// Exponent offset of the score pass: each term is formed as
+// 2^(24 + (logit - lse) log2 e) and the sum is scaled by 2^-24 at the end, so
+// the fast base-2 exponential (which flushes results below 2^-126) still
+// yields every term that is representable in fp32 after the scaling.
+constexpr float kExpOffset = 24.f;
+
+// Accumulates this thread's positions t0 + threadIdx.x + e*kScoreThreads over
+// the (padded) rows; kWhole: every position is inside the row.
+template <bool kWhole>
+__device__ __forceinline__ void score_rows(const TopkParams &p, const float *s_c, const long long *s_row,
+                                           int nrows_pad, int t0, int L, float (&acc)[kScorePerThread]) {
+    const float *base = p.logits + t0 + threadIdx.x;
+    for (int i0 = 0; i0 < nrows_pad; i0 += kScoreRowBatch) {
+        float x[kScoreRowBatch][kScorePerThread];
+#pragma unroll
+        for (int ii = 0; ii < kScoreRowBatch; ++ii) {
+            const float *row = base + s_row[i0 + ii];
+#pragma unroll
+            for (int e = 0; e < kScorePerThread; ++e)
+                x[ii][e] = (kWhole || t0 + e * kScoreThreads + (int)threadIdx.x < L) ? __ldcs(row + e * kScoreThreads)
+                                                                                      : neg_inf();
+        }
+#pragma unroll
+        for (int ii = 0; ii < kScoreRowBatch; ++ii) {
+            const float c = s_c[i0 + ii];
+#pragma unroll
+            for (int e = 0; e < kScorePerThread; ++e) acc[e] += ex2_approx(fmaf(x[ii][e], kLog2e, c));
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kScoreThreads) topk_scores_kernel(const TopkParams p) {
@@ -100,43 +117,32 @@ __global__ void __launch_bounds__(kScoreThreads) topk_scores_kernel(const TopkPa
     long long lg_off, sc_off;
     verify_offsets(p, v, &lg_off, &sc_off);
     const int R = p.row_hi - p.row_lo, nrows = R * p.G;
-    __shared__ float s_lse[kMaxRows];
+    const int nrows_pad = (nrows + kScoreRowBatch - 1) / kScoreRowBatch * kScoreRowBatch;
+    // per averaged row: its offset in the logits and 24 - lse*log2(e); the
+    // padding rows repeat row 0's offset and contribute 2^-inf = 0
+    __shared__ float s_c[kMaxRows];
     __shared__ long long s_row[kMaxRows];
-    for (int i = threadIdx.x; i < nrows; i += blockDim.x) {
-        const int h = g * p.G + i / R, r = p.row_lo + i % R;
-        s_lse[i] = p.lse[((long long)v * p.Hq + h) * (p.k + 1) + r];
+    static_assert(kMaxRows % kScoreRowBatch == 0 && kMaxRows <= kScoreThreads, "row tables");
+    if (threadIdx.x < nrows_pad) {
+        const int i = threadIdx.x, ir = i < nrows ? i : 0;
+        const int h = g * p.G + ir / R, r = p.row_lo + ir % R;
+        s_c[i] = i < nrows ? kExpOffset - p.lse[((long long)v * p.Hq + h) * (p.k + 1) + r] * kLog2e : neg_inf();
         s_row[i] = lg_off + ((long long)h * (p.k + 1) + r) * L;
     }
     __syncthreads();
     float acc[kScorePerThread];
 #pragma unroll
     for (int e = 0; e < kScorePerThread; ++e) acc[e] = 0.f;
-    const bool whole = t0 + kScoreChunk <= L;  // no position of this chunk is past the row's end
-    for (int i0 = 0; i0 < nrows; i0 += kScoreRowBatch) {
-        float x[kScoreRowBatch][kScorePerThread];
-#pragma unroll
-        for (int ii = 0; ii < kScoreRowBatch; ++ii) {
-            const int i = i0 + ii;
-            const float *row = p.logits + (i < nrows ? s_row[i] : 0ll) + t0 + threadIdx.x;
-#pragma unroll
-            for (int e = 0; e < kScorePerThread; ++e) {
-                const bool in = i < nrows && (whole || t0 + e * kScoreThreads + (int)threadIdx.x < L);
-                x[ii][e] = in ? __ldcs(row + e * kScoreThreads) : neg_inf();
-            }
-        }
-#pragma unroll
-        for (int ii = 0; ii < kScoreRowBatch; ++ii) {
-            const float ls = i0 + ii < nrows ? s_lse[i0 + ii] : 0.f;
-#pragma unroll
-            for (int e = 0; e < kScorePerThread; ++e) acc[e] += exp2_sub((x[ii][e] - ls) * kLog2e);
-        }
-    }
-    const float denom = (float)(R * p.G);
+    if (t0 + kScoreChunk <= L)
+        score_rows<true>(p, s_c, s_row, nrows_pad, t0, L, acc);
+    else
+        score_rows<false>(p, s_c, s_row, nrows_pad, t0, L, acc);
+    const float scale = 0x1p-24f / (float)nrows;  // undo the exponent offset; mean over the R*G rows
     float *dst = p.scores + sc_off + (long long)g * L;
 #pragma unroll
     for (int e = 0; e < kScorePerThread; ++e) {
         const int t = t0 + e * kScoreThreads + threadIdx.x;
-        if (t < L) dst[t] = acc[e] / denom;
+        if (t < L) dst[t] = acc[e] * scale;
     }
 }
 
