@@ -267,3 +267,34 @@ def test_topk_budget_edges_and_ties():
     ref = oracle.topk_select(Hq=Hq, Hkv=Hkv, k=k, row_lo=1, row_hi=k + 1, logits=lg.ravel().astype(np.float64),
                              lse=lse.astype(np.float64), L=[L] * V, K=[2, 0, 64], max_topk=64)
     compare_topk(ni, nc, ref, [L] * V, [2, 0, 64], Hkv)
+
+
+@pytest.mark.parametrize("L,K,n_tied", [(50000, 2500, 0), (12000, 3000, 6000), (45000, 2000, 5000)])
+def test_topk_long_rows_and_wide_ties(L, K, n_tied):
+    """Rows longer than the select's shared-memory key buffer (keys stay in
+    global memory) and thousands of exactly tied scores (more keys in the
+    threshold's first digit than the candidate buffer holds): the sets match
+    the oracle's, ties go to the lowest positions."""
+    V, Hq, Hkv, k = 1, 4, 2, 2
+    rng = np.random.default_rng(L + n_tied)
+    lg = rng.standard_normal((V, Hq, k + 1, L)).astype(np.float32)
+    if n_tied:
+        cols = np.sort(rng.choice(L, n_tied, replace=False))
+        lg[0, :, :, cols] = 3.5  # identical columns: bitwise-equal scores
+    lse = np.log(np.exp(lg.astype(np.float64)).sum(-1)).astype(np.float32)
+    import sparse_self_speculative_pillar_gb300 as P
+    shape = P.make_shape(B=V, Hq=Hq, Hkv=Hkv, D=64, k=k, max_sparse=1, max_len=L, num_slots=1, max_topk=K)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    nidx = torch.full((V, Hkv, K), -1, dtype=torch.int32, device="cuda")
+    ncnt = torch.full((V, Hkv), -1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(P.pillar_topk_workspace_bytes(shape, V), dtype=torch.uint8, device="cuda")
+    P.pillar_topk_select(shape, V, dev(lg.ravel()), dev(lse), dev(np.full(V, L, np.int32)),
+                         dev(np.arange(V, dtype=np.int32)), dev(np.array([K], np.int32)), nidx, ncnt, ws)
+    assert P.pillar_get_error(ws) == 0
+    ni, nc = nidx.cpu().numpy(), ncnt.cpu().numpy()
+    ref = oracle.topk_select(Hq=Hq, Hkv=Hkv, k=k, row_lo=1, row_hi=k + 1, logits=lg.ravel().astype(np.float64),
+                             lse=lse.astype(np.float64), L=[L], K=[K], max_topk=K)
+    compare_topk(ni, nc, ref, [L], [K], Hkv)
+    if n_tied >= K:  # every kept position is one of the tied columns, the lowest ones
+        for g in range(Hkv):
+            np.testing.assert_array_equal(ni[0, g, :K], cols[:K])
