@@ -67,7 +67,8 @@ struct AttnParams {
     const ReqInfo *req;
     const long long *kv_off, *logit_off;
     const UnitInfo *unit;
-    const int *merge_list;
+    const MergeUnit *merge_units;
+    int merge_cap;  // merge-unit slots in the workspace
     const Item *items;
     float *part_o, *part_lse;
     long long num_slots;
@@ -867,42 +868,39 @@ __global__ void __launch_bounds__(kThreads, 1) unified_attn_kernel(const __grid_
 // ============================================================== merge of partials
 
 constexpr int kMergeThreads = 128;
-constexpr int kMergeBatch = 8;   // records whose loads are in flight together
+constexpr int kMergeBatch = 8;     // records whose loads are in flight together
+constexpr int kMergeCtasPerSm = 8;  // grid: one task per thread for the usual sizes, all CTAs resident
 
 // Combines the partial rows of every split (request, KV head).  A split unit
-// has nsplit records of rec_rows rows (M for verify, G for draft); the work is
+// has nrec records of nrows rows (M for verify, G for draft); the work is
 // flattened over (listed unit, row, four output dimensions), one thread each,
-// so that few, long units still spread over the whole GPU.  A thread merges
-// its records in batches (all loads of a batch in flight), carrying a running
+// so that few, long units still spread over the whole GPU.  The planner's
+// MergeUnit record holds everything a task needs, so a thread issues its
+// record's load together with the unit count and then all its partials'
+// loads at once.  A thread merges its records in batches, carrying a running
 // max and sums between batches.
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p) {
     pdl_wait_prerequisites();  // the partials come from the attention kernel
-    const int nm = p.hdr->num_merge;
     const int per_unit = p.M * (D / 4);  // thread slots per listed unit (rows up to M)
-    const long long total = (long long)nm * per_unit;
-    for (long long w = (long long)blockIdx.x * kMergeThreads + threadIdx.x; w < total;
+    for (long long w = (long long)blockIdx.x * kMergeThreads + threadIdx.x; w < (long long)p.merge_cap * per_unit;
          w += (long long)gridDim.x * kMergeThreads) {
         const int li = (int)(w / per_unit);
         const int idx = (int)(w - (long long)li * per_unit);
-        const int u = p.merge_list[li];
-        const UnitInfo ui = p.unit[u];
-        const int nrows = ui.rec_rows, nrec = ui.nsplit;
+        const MergeUnit mu = p.merge_units[li];  // in flight with the count below (stale past it: unused)
+        if (li >= p.hdr->num_merge) break;      // li only grows along the loop
         const int row = idx / (D / 4), c4 = idx - row * (D / 4);
-        if (row >= nrows) continue;
-        const int b = u / p.Hkv, g = u - b * p.Hkv;
-        const ReqInfo ri = p.req[b];
-        const bool verify = ri.mode == 1;
+        if (row >= mu.nrows) continue;
         float mx = neg_inf(), den = 0.f;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int r0 = 0; r0 < nrec; r0 += kMergeBatch) {
+        for (int r0 = 0; r0 < mu.nrec; r0 += kMergeBatch) {
             float ls[kMergeBatch];
             float4 v[kMergeBatch];
 #pragma unroll
             for (int q = 0; q < kMergeBatch; ++q) {
                 const int r = r0 + q;
-                if (r < nrec) {
-                    const size_t pr = (size_t)ui.rec_base + (size_t)r * nrows + row;
+                if (r < mu.nrec) {
+                    const size_t pr = (size_t)mu.rec_base + (size_t)r * mu.nrows + row;
                     ls[q] = __ldcg(p.part_lse + pr);
                     v[q] = __ldcg(reinterpret_cast<const float4 *>(p.part_o + pr * D) + c4);
                 } else {
@@ -914,12 +912,12 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p
 #pragma unroll
             for (int q = 0; q < kMergeBatch; ++q) bm = fmaxf(bm, ls[q]);
             if (bm == neg_inf()) continue;
-            const float a = expf(mx - bm);  // rescale what was merged so far (0 when empty)
+            const float a = ex2_approx((mx - bm) * kLog2e);  // rescale what was merged so far (0 when empty)
             den *= a;
             o = make_float4(o.x * a, o.y * a, o.z * a, o.w * a);
 #pragma unroll
             for (int q = 0; q < kMergeBatch; ++q) {
-                const float wq = expf(ls[q] - bm);
+                const float wq = ex2_approx((ls[q] - bm) * kLog2e);
                 den += wq;
                 o.x += wq * v[q].x;
                 o.y += wq * v[q].y;
@@ -934,17 +932,13 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p
             o = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
             lse = mx + logf(den);
         }
-        int j = 0, gi = row;
-        if (verify) {
-            j = row / p.G;
-            gi = row - j * p.G;
-        }
-        const size_t orow = (size_t)(ri.q_off + j) * p.Hq + (size_t)g * p.G + gi;
+        const int j = mu.verify ? row / p.G : 0, gi = row - j * p.G;
+        const long long orow = mu.orow0 + (long long)j * p.Hq + gi;
         uint2 pk;
         pk.x = pack_bf16x2(o.x, o.y);
         pk.y = pack_bf16x2(o.z, o.w);
         *reinterpret_cast<uint2 *>(p.out + orow * D + 4 * c4) = pk;
-        if (verify && c4 == 0) p.lse[((size_t)ri.vidx * p.Hq + (size_t)g * p.G + gi) * (p.k + 1) + j] = lse;
+        if (mu.verify && c4 == 0) p.lse[mu.lse0 + (long long)gi * (p.k + 1) + j] = lse;
     }
 }
 
@@ -981,7 +975,7 @@ cudaError_t launch_unified_t(const AttnParams &p, int nsm, cudaStream_t st) {
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, unified_attn_kernel<D>, p);
     if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(nsm * 16);
+    cfg.gridDim = dim3(nsm * kMergeCtasPerSm);
     cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     return cudaLaunchKernelEx(&cfg, merge_kernel<D>, p);
@@ -1038,7 +1032,8 @@ cudaError_t launch_attn(const AttnArgs &a, int nsm, cudaStream_t st) {
     p.kv_off = reinterpret_cast<const long long *>(a.ws + a.lay.kv_off);
     p.logit_off = reinterpret_cast<const long long *>(a.ws + a.lay.logit_off);
     p.unit = reinterpret_cast<const UnitInfo *>(a.ws + a.lay.unit);
-    p.merge_list = reinterpret_cast<const int *>(a.ws + a.lay.merge_list);
+    p.merge_units = reinterpret_cast<const MergeUnit *>(a.ws + a.lay.merge_units);
+    p.merge_cap = (int)((a.lay.items - a.lay.merge_units) / sizeof(MergeUnit));
     p.items = reinterpret_cast<const Item *>(a.ws + a.lay.items);
     p.part_o = reinterpret_cast<float *>(a.ws + a.lay.part_o);
     p.part_lse = reinterpret_cast<float *>(a.ws + a.lay.part_lse);

@@ -37,6 +37,17 @@ struct UnitInfo {
     int rec_rows;   // partial rows written per item of a split unit: M (verify), G (draft); 0 if not split
 };
 
+// A split (request, KV head) as the merge sees it: where its partial rows
+// are and where the combined rows go.
+struct MergeUnit {
+    int rec_base;    // first partial row of its first item
+    int nrows;       // rows per item: M (verify), G (draft)
+    int nrec;        // items (partial records per row)
+    int verify;
+    long long orow0;  // output row of its row 0: q_off*Hq + g*G (row j*G + gi -> orow0 + j*Hq + gi)
+    long long lse0;   // verify: LSE index of its row 0, (vidx*Hq + g*G)*(k+1) (row j*G + gi -> lse0 + gi*(k+1) + j)
+};
+
 struct Item {
     int unit;       // b * Hkv + g
     int begin;      // first key (verify: position; draft: list index)
@@ -55,7 +66,7 @@ struct WsHeader {
 
 // Byte offsets of the attention workspace sections.
 struct AttnLayout {
-    size_t req, kv_off, logit_off, unit, merge_list, items, part_o, part_lse, total;
+    size_t req, kv_off, logit_off, unit, merge_units, items, part_o, part_lse, total;
     long long max_items, max_rec_rows;
 };
 
@@ -84,7 +95,7 @@ inline AttnLayout attn_layout(const pillar_shape_t &s) {
     l.kv_off = off;     off = align256(off + sizeof(long long) * B);
     l.logit_off = off;  off = align256(off + sizeof(long long) * B);
     l.unit = off;       off = align256(off + sizeof(UnitInfo) * U);
-    l.merge_list = off; off = align256(off + sizeof(int) * U);
+    l.merge_units = off; off = align256(off + sizeof(MergeUnit) * U);
     l.items = off;      off = align256(off + sizeof(Item) * l.max_items);
     l.part_o = off;     off = align256(off + sizeof(float) * (size_t)l.max_rec_rows * s.D);
     l.part_lse = off;   off = align256(off + sizeof(float) * (size_t)l.max_rec_rows);

@@ -28,7 +28,7 @@ struct PlanParams {
     ReqInfo *req;
     long long *kv_off, *logit_off;
     UnitInfo *unit;
-    int *merge_list;
+    MergeUnit *merge_units;
     Item *items;
     int B, Hq, Hkv, k, max_sparse, max_len, vchunk, dchunk;
 };
@@ -177,7 +177,21 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
             // draft bases are relative here; the verify total is added below
             ui.item_base = (int)(r.mode == 1 ? carry[4] + v[4] : carry[5] + v[5]);
             p.unit[u] = ui;
-            if (rec_rows > 0) p.merge_list[carry[7] + v[7]] = u;
+            if (rec_rows > 0) {
+                // the request's first query row and verify index: the exclusive prefixes at
+                // its g = 0 unit, which precedes this one in the scan
+                const int qrows = r.mode == 1 ? p.k + 1 : 1;
+                const long long q_off = carry[0] + v[0] - (g > 0 ? qrows : 0);
+                const long long vidx = carry[2] + v[2] - (g > 0 ? (r.mode == 1) : 0);
+                MergeUnit mu;
+                mu.rec_base = ui.rec_base;
+                mu.nrows = rec_rows;
+                mu.nrec = ns;
+                mu.verify = r.mode == 1;
+                mu.orow0 = q_off * p.Hq + (long long)g * G;
+                mu.lse0 = r.mode == 1 ? (vidx * p.Hq + (long long)g * G) * (p.k + 1) : -1;
+                p.merge_units[carry[7] + v[7]] = mu;
+            }
         }
 #pragma unroll
         for (int i = 0; i < kScanN; ++i) carry[i] += tot[i];
@@ -228,7 +242,7 @@ cudaError_t launch_plan(const PlanArgs &a, cudaStream_t st) {
     p.kv_off = reinterpret_cast<long long *>(a.ws + a.lay.kv_off);
     p.logit_off = reinterpret_cast<long long *>(a.ws + a.lay.logit_off);
     p.unit = reinterpret_cast<UnitInfo *>(a.ws + a.lay.unit);
-    p.merge_list = reinterpret_cast<int *>(a.ws + a.lay.merge_list);
+    p.merge_units = reinterpret_cast<MergeUnit *>(a.ws + a.lay.merge_units);
     p.items = reinterpret_cast<Item *>(a.ws + a.lay.items);
     p.B = a.B;
     p.Hq = a.Hq;
