@@ -233,6 +233,37 @@ def run_reference(args):
     return 0
 
 
+# --------------------------------------------------------------------------- replicas (N > 1)
+# The path shards by request and KV head with no exchange step, so N GPUs run
+# N replicas: each rank times its own seeded replica, the ranks meet only at
+# the timing barriers, and the whole-job value divides the slowest rank's time
+# by the layer-steps of all ranks.
+
+def replica_recipe(args, rank):
+    """The workload recipe of one rank: the named one on rank 0 (unless scaled
+    for a profiling run), a distinct seed of the same shape elsewhere."""
+    if rank or args.length_scale != 1.0 or args.batch:
+        return W.scaled(args.workload, B=args.batch, length_scale=args.length_scale, seed_offset=1000 * rank)
+    return W.RECIPES[args.workload]
+
+
+def max_over_ranks(x, world, device):
+    """The maximum of a per-rank float over the process group (x itself when alone)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_us(max_elapsed_ms, steps, world):
+    """Microseconds per layer-step of the whole job: every rank ran `steps`
+    layer-steps of its replica in at most max_elapsed_ms."""
+    return max_elapsed_ms * 1e3 / (steps * world)
+
+
 # --------------------------------------------------------------------------- GPU arm
 
 def run_gpu(args):
@@ -247,11 +278,7 @@ def run_gpu(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     P.load()
 
-    # each rank: its own replica of the workload (distinct seed)
-    rec = W.RECIPES[args.workload]
-    if rank or args.length_scale != 1.0 or args.batch:
-        rec = W.scaled(args.workload, B=args.batch, length_scale=args.length_scale, seed_offset=1000 * rank)
-    w = W.generate(rec)
+    w = W.generate(replica_recipe(args, rank))  # each rank: its own replica of the workload
     g = Gpu(w)
     ab = W.algorithmic_bytes(w)
     stream = torch.cuda.current_stream()
@@ -283,12 +310,8 @@ def run_gpu(args):
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
-    elapsed_ms = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-    us_per_step = elapsed_ms * 1e3 / (args.steps * world)
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop), world, "cuda")
+    us_per_step = whole_job_us(elapsed_ms, args.steps, world)
     if args.quick:
         if rank == 0:
             print(json.dumps({"metric": METRIC, "value": us_per_step, "unit": UNIT, "n_gpus": world,
@@ -333,12 +356,8 @@ def run_gpu(args):
             t.copy_(getattr(g, n), non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_us = e2e_ms * 1e3 / (e2e_steps * world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, "cuda")
+    e2e_us = whole_job_us(e2e_ms, e2e_steps, world)
     flags = g.attn_flags() | g.topk_flags()
 
     if rank != 0:
