@@ -122,7 +122,7 @@ struct Smem {
     static constexpr int off_meta = off_info + kRowLists * (int)sizeof(ItemInfo);
     static constexpr int off_pend = off_meta + kMaxStages * (int)sizeof(StageMeta);
     static constexpr int off_bar = off_pend + kSBuf * 16;
-    // full[8], empty[8], qempty[2], rfull[3], rempty[3], s_full[4], s_free[4], p_full[4], o_free[2], cexit, drain
+    // full[8], empty[8], qempty[2], rfull[4], rempty[4], s_full[4], s_free[4], p_full[4], o_free[2], cexit, drain
     static constexpr int NBAR = 2 * kMaxStages + 2 + 2 * kRowLists + 3 * kSBuf + 2 + 2;
     static constexpr int off_misc = off_bar + NBAR * 8;
     static constexpr int off_stage = (off_misc + 16 + 1023) / 1024 * 1024;

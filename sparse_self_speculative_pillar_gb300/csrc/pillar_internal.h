@@ -18,7 +18,7 @@ constexpr int kMaxRows = 64;           // (k+1)*G bound of a verify tile
 constexpr int kMaxG = 8;               // query heads per KV head
 constexpr int kDefaultVerifyChunk = 1024;
 constexpr int kDefaultDraftChunk = 1024;
-constexpr int kMaxChunk = 1024;        // item key bound (sizes the two row lists in shared memory)
+constexpr int kMaxChunk = 1024;        // item key bound (sizes the resolved row lists in shared memory)
 constexpr int kPlanThreads = 1024;
 constexpr unsigned long long kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
