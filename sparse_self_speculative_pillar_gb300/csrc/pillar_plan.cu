@@ -57,15 +57,23 @@ __device__ void block_scan8(long long (&v)[kScanN], long long (&tot)[kScanN]) {
     }
     __syncthreads();
     if (wid == 0) {
+        // the columns in two halves, each loaded first and scanned together:
+        // independent shuffle chains within the 64 registers a thread has here
 #pragma unroll
-        for (int i = 0; i < kScanN; ++i) {
-            long long t = warp_sums[lane][i];
+        for (int h = 0; h < kScanN; h += kScanN / 2) {
+            long long t[kScanN / 2];
+#pragma unroll
+            for (int i = 0; i < kScanN / 2; ++i) t[i] = warp_sums[lane][h + i];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const long long y = __shfl_up_sync(0xffffffffu, t, o);
-                if (lane >= o) t += y;
+#pragma unroll
+                for (int i = 0; i < kScanN / 2; ++i) {
+                    const long long y = __shfl_up_sync(0xffffffffu, t[i], o);
+                    if (lane >= o) t[i] += y;
+                }
             }
-            warp_sums[lane][i] = t;
+#pragma unroll
+            for (int i = 0; i < kScanN / 2; ++i) warp_sums[lane][h + i] = t[i];
         }
     }
     __syncthreads();
@@ -92,25 +100,24 @@ __device__ __forceinline__ int chunking(int n, int chunk, int *ns) {
     return cs;
 }
 
-// Keys, split count and chunk size of unit u of a request with record r.
-__device__ __forceinline__ int unit_split(const PlanParams &p, const ReqInfo &r, int u, int *n, int *ns, int *bad) {
+// Keys, split count and chunk size of a unit of a request with record r;
+// cnt is the unit's sparse_cnt entry (used by draft units only).
+__device__ __forceinline__ int unit_split(const PlanParams &p, const ReqInfo &r, int cnt, int *n, int *ns, int *bad) {
     if (r.mode == 1) {
         *n = r.len;
         return chunking(r.len, p.vchunk, ns);
     }
-    int c = r.mode == 0 ? p.sparse_cnt[u] : 0;
+    int c = r.mode == 0 ? cnt : 0;
     if (c < 0 || c > p.max_sparse) *bad |= PILLAR_FLAG_COUNT;
     c = c < 0 ? 0 : (c > p.max_sparse ? p.max_sparse : c);
     *n = c;
     return chunking(c, p.dchunk, ns);
 }
 
-// Request record of request b (validated).
-__device__ __forceinline__ ReqInfo read_request(const PlanParams &p, int b, int *bad, int *len_out) {
+// Request record from a request's mode and length (validated).
+__device__ __forceinline__ ReqInfo check_request(const PlanParams &p, int mode, int len, int *bad, int *len_out) {
     ReqInfo r;
     r.q_off = r.vidx = 0;
-    const int mode = p.req_mode[b];
-    int len = p.req_len[b];
     r.mode = mode;
     if (mode != 0 && mode != 1) *bad |= PILLAR_FLAG_REQUEST, r.mode = -1;
     if (len < 0) *bad |= PILLAR_FLAG_REQUEST, len = 0;
@@ -119,6 +126,25 @@ __device__ __forceinline__ ReqInfo read_request(const PlanParams &p, int b, int 
     if (r.mode == 1 && len < p.k + 1) *bad |= PILLAR_FLAG_REQUEST;
     *len_out = len;
     return r;
+}
+
+// The work items of unit u.  A verify request's Hkv units all have ns items;
+// they are listed chunk by chunk, head-minor (request, chunk, head), so the
+// Hkv items reading the same positions are taken up together.  Draft items
+// stay per unit.
+__device__ __forceinline__ void emit_items(const PlanParams &p, int u, const ReqInfo &r, int n, int ns, int cs,
+                                           int item_base) {
+    const int g = u - (u / p.Hkv) * p.Hkv;
+    const int first = r.mode == 1 ? item_base - g * ns + g : item_base;
+    const int step = r.mode == 1 ? p.Hkv : 1;
+    for (int s = 0; s < ns; ++s) {
+        Item it;
+        it.unit = u;
+        it.begin = s * cs;
+        it.end = min(n, (s + 1) * cs);
+        it.split = s;
+        p.items[first + s * step] = it;
+    }
 }
 
 // One thread per unit (request, KV head), chunks of kPlanThreads units; the
@@ -136,19 +162,30 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
         p.hdr->item_counter = 0;
     }
     int bad = 0;
-    // running totals: q rows, kv positions, verify requests, logits, verify items, draft items, partial rows, merges
-    long long carry[kScanN] = {0, 0, 0, 0, 0, 0, 0, 0};
+    // When one chunk covers every unit (U <= kPlanThreads), each thread keeps
+    // its unit's record and emits its items without reading anything back.
+    const bool one_chunk = U <= kPlanThreads;
+    ReqInfo r1;
+    int n1 = 0, ns1 = 1, cs1 = 0, item1 = 0;
+    // running totals of the chunks before (shared memory: no registers held across the scans):
+    // q rows, kv positions, verify requests, logits, verify items, draft items, partial rows, merges
+    __shared__ long long carry[kScanN];
+    if (tid < kScanN) carry[tid] = 0;
+    __syncthreads();
     for (int base = 0; base < U; base += kPlanThreads) {
         const int u = base + tid;
         const bool live = u < U;
         const int b = live ? u / p.Hkv : 0, g = live ? u - b * p.Hkv : 0;
+        // the unit's three inputs in one round trip
+        const int in_mode = live ? p.req_mode[b] : 0, in_len = live ? p.req_len[b] : 0;
+        const int in_cnt = live ? p.sparse_cnt[u] : 0;
         long long v[kScanN] = {0, 0, 0, 0, 0, 0, 0, 0};
         ReqInfo r;
-        int len = 0, n = 0, ns = 1, rec_rows = 0;
+        int len = 0, n = 0, ns = 1, cs = 0, rec_rows = 0;
         if (live) {
             int ignored = 0;
-            r = read_request(p, b, g == 0 ? &bad : &ignored, &len);  // request problems are flagged once
-            unit_split(p, r, u, &n, &ns, &bad);
+            r = check_request(p, in_mode, in_len, g == 0 ? &bad : &ignored, &len);  // request problems flagged once
+            cs = unit_split(p, r, in_cnt, &n, &ns, &bad);
             rec_rows = ns > 1 ? (r.mode == 1 ? M : G) : 0;
             if (g == 0) {
                 v[0] = r.mode == 1 ? p.k + 1 : 1;
@@ -174,9 +211,17 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
             ui.nsplit = ns;
             ui.rec_rows = rec_rows;
             ui.rec_base = (int)(carry[6] + v[6]);
-            // draft bases are relative here; the verify total is added below
-            ui.item_base = (int)(r.mode == 1 ? carry[4] + v[4] : carry[5] + v[5]);
+            // draft items follow every verify item: with one chunk the verify total is
+            // known here, otherwise the bases are relative and fixed up below
+            ui.item_base = (int)(r.mode == 1 ? carry[4] + v[4] : carry[5] + v[5] + (one_chunk ? tot[4] : 0));
             p.unit[u] = ui;
+            if (one_chunk) {
+                r1 = r;
+                n1 = n;
+                ns1 = ns;
+                cs1 = cs;
+                item1 = ui.item_base;
+            }
             if (rec_rows > 0) {
                 // the request's first query row and verify index: the exclusive prefixes at
                 // its g = 0 unit, which precedes this one in the scan
@@ -193,8 +238,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
                 p.merge_units[carry[7] + v[7]] = mu;
             }
         }
+        __syncthreads();  // every thread has read this chunk's carries
+        if (tid == 0) {
 #pragma unroll
-        for (int i = 0; i < kScanN; ++i) carry[i] += tot[i];
+            for (int i = 0; i < kScanN; ++i) carry[i] += tot[i];
+        }
+        __syncthreads();
     }
     const long long ver_items = carry[4];
     if (tid == 0) {
@@ -202,31 +251,22 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
         p.hdr->num_units = U;
         p.hdr->num_merge = (int)carry[7];
     }
-    // Emit the items (each thread re-reads only the unit it wrote itself).
-    for (int u = tid; u < U; u += kPlanThreads) {
-        const int b = u / p.Hkv;
-        int len, dummy = 0;
-        const ReqInfo r = read_request(p, b, &dummy, &len);
-        UnitInfo ui = p.unit[u];
-        if (r.mode != 1) {
-            ui.item_base += (int)ver_items;
-            p.unit[u].item_base = ui.item_base;
-        }
-        int n, ns;
-        const int cs = unit_split(p, r, u, &n, &ns, &dummy);
-        // A verify request's Hkv units all have ns items; they are listed chunk
-        // by chunk, head-minor (request, chunk, head), so the Hkv items reading
-        // the same positions are taken up together.  Draft items stay per unit.
-        const int g = u - b * p.Hkv;
-        const int first = r.mode == 1 ? ui.item_base - g * ns + g : ui.item_base;
-        const int step = r.mode == 1 ? p.Hkv : 1;
-        for (int s = 0; s < ns; ++s) {
-            Item it;
-            it.unit = u;
-            it.begin = s * cs;
-            it.end = min(n, (s + 1) * cs);
-            it.split = s;
-            p.items[first + s * step] = it;
+    // Emit the items.
+    if (one_chunk) {
+        if (tid < U) emit_items(p, tid, r1, n1, ns1, cs1, item1);
+    } else {
+        for (int u = tid; u < U; u += kPlanThreads) {  // each thread re-reads only the unit it wrote itself
+            const int b = u / p.Hkv;
+            int len, dummy = 0;
+            const ReqInfo r = check_request(p, p.req_mode[b], p.req_len[b], &dummy, &len);
+            UnitInfo ui = p.unit[u];
+            if (r.mode != 1) {
+                ui.item_base += (int)ver_items;
+                p.unit[u].item_base = ui.item_base;
+            }
+            int n, ns;
+            const int cs = unit_split(p, r, p.sparse_cnt[u], &n, &ns, &dummy);
+            emit_items(p, u, r, n, ns, cs, ui.item_base);
         }
     }
     if (bad) atomicOr(&p.hdr->err, bad);
