@@ -867,9 +867,9 @@ __global__ void __launch_bounds__(kThreads, 1) unified_attn_kernel(const __grid_
 
 // ============================================================== merge of partials
 
-constexpr int kMergeThreads = 128;
-constexpr int kMergeBatch = 8;     // records whose loads are in flight together
-constexpr int kMergeCtasPerSm = 8;  // grid: one task per thread for the usual sizes, all CTAs resident
+constexpr int kMergeThreads = 1024;
+constexpr int kMergeBatch = 4;     // records whose loads are in flight together
+constexpr int kMergeCtasPerSm = 1;  // one large CTA per SM: the whole grid is resident when the attention kernel ends
 
 // Combines the partial rows of every split (request, KV head).  A split unit
 // has nrec records of nrows rows (M for verify, G for draft); the work is
@@ -880,7 +880,7 @@ constexpr int kMergeCtasPerSm = 8;  // grid: one task per thread for the usual s
 // loads at once.  A thread merges its records in batches, carrying a running
 // max and sums between batches.
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(const AttnParams p) {
     pdl_wait_prerequisites();  // the partials come from the attention kernel
     const int per_unit = p.M * (D / 4);  // thread slots per listed unit (rows up to M)
     for (long long w = (long long)blockIdx.x * kMergeThreads + threadIdx.x; w < (long long)p.merge_cap * per_unit;
