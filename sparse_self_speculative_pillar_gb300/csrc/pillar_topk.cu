@@ -146,32 +146,33 @@ __global__ void __launch_bounds__(kScoreThreads) topk_scores_kernel(const TopkPa
     }
 }
 
-// Exclusive scan of one int per thread over the select block.
-__device__ int select_block_scan(int v, int *total) {
-    __shared__ int ws[kSelectThreads / 32];
+// Exclusive scans of two ints per thread over the select block, together
+// (one set of shuffles and barriers); *total gets the block totals.
+__device__ int2 select_block_scan2(int a, int b, int2 *total) {
+    __shared__ int2 ws[kSelectWarps];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    int x = v;
+    int xa = a, xb = b;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+        const int ya = __shfl_up_sync(0xffffffffu, xa, o), yb = __shfl_up_sync(0xffffffffu, xb, o);
+        if (lane >= o) xa += ya, xb += yb;
     }
-    if (lane == 31) ws[wid] = x;
+    if (lane == 31) ws[wid] = make_int2(xa, xb);
     __syncthreads();
     if (wid == 0) {
-        int s = ws[lane];
+        int2 t = ws[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += y;
+            const int ya = __shfl_up_sync(0xffffffffu, t.x, o), yb = __shfl_up_sync(0xffffffffu, t.y, o);
+            if (lane >= o) t.x += ya, t.y += yb;
         }
-        ws[lane] = s;
+        ws[lane] = t;
     }
     __syncthreads();
-    const int base = wid ? ws[wid - 1] : 0;
-    *total = ws[kSelectThreads / 32 - 1];
+    const int2 base = wid ? ws[wid - 1] : make_int2(0, 0);
+    *total = ws[kSelectWarps - 1];
     __syncthreads();
-    return base + x - v;
+    return make_int2(base.x + xa - a, base.y + xb - b);
 }
 
 __device__ __forceinline__ uint32_t score_key(float s) { return __float_as_uint(s) & 0x7fffffffu; }
@@ -183,12 +184,19 @@ __global__ void __launch_bounds__(kSelectThreads, 1) topk_select_kernel(const To
     __shared__ uint32_t s_prefix, s_mask, s_remaining;
     pdl_wait_prerequisites();  // the scores (and everything before them) are complete and visible
     const int v = blockIdx.y, g = blockIdx.x, tid = threadIdx.x;
-    const int L = p.req_len[p.group_map[v]];
+    __shared__ int s_lk[2];
+    if (tid == 32) {  // the request's length and budget, read while warp 0 sums the offsets
+        s_lk[0] = p.req_len[p.group_map[v]];
+        s_lk[1] = p.K[v];
+    }
+    long long lg_off, sc_off;
+    verify_offsets(p, v, &lg_off, &sc_off);  // ends with a block barrier
+    const int L = s_lk[0];
     if (L < 0 || L > p.max_len) {
         if (tid == 0) p.next_cnt[v * p.Hkv + g] = 0;
         return;
     }
-    int K = p.K[v];
+    int K = s_lk[1];
     K = K < 0 ? 0 : (K > L ? L : K);
     if (K > p.max_topk) {
         if (tid == 0) atomicOr(&p.hdr->err, PILLAR_FLAG_TOPK);
@@ -201,8 +209,6 @@ __global__ void __launch_bounds__(kSelectThreads, 1) topk_select_kernel(const To
         for (int t = tid; t < L; t += blockDim.x) dst[t] = t;
         return;
     }
-    long long lg_off, sc_off;
-    verify_offsets(p, v, &lg_off, &sc_off);
     const float *sc = p.scores + sc_off + (long long)g * L;
     const uint32_t *keys;
     if (L <= p.smem_keys) {
@@ -296,9 +302,9 @@ __global__ void __launch_bounds__(kSelectThreads, 1) topk_select_kernel(const To
         cgt += key > T;
         ceq += key == T;
     }
-    int tot_gt, tot_eq;
-    const int gt_before = select_block_scan(cgt, &tot_gt);
-    const int eq_before = select_block_scan(ceq, &tot_eq);
+    int2 tot;
+    const int2 before = select_block_scan2(cgt, ceq, &tot);
+    const int gt_before = before.x, eq_before = before.y;
     int out = gt_before + min(eq_before, need_eq);
     int eq_rank = eq_before;
     for (int t = tb; t < te; ++t) {
