@@ -273,6 +273,23 @@ __device__ void resolver(const AttnParams &p, const Ctx &c, int lane) {
     }
 }
 
+// L2 cache policy: lines of a single-use stream, evicted before other lines.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_gather4 with an L2 cache policy for the rows it reads.
+__device__ __forceinline__ void tma_gather4_hint(void *dst, const void *tmap, int col, int r0, int r1, int r2, int r3,
+                                                 uint64_t *bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+        "[%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
 // ============================================================== loader warps
 
 // The loader warps share every tile: warp li fetches rows [RW li, RW li + RW),
@@ -295,6 +312,9 @@ __device__ void loader(const AttnParams &p, const Ctx &c, int lane, int li) {
     // this lane's gather4: row group rgl of the warp's rows, K (kv 0) or V (kv 1), column half h
     const int rgl = lane % GW, kv = (lane / GW) & 1, h = lane / (2 * GW);
     const bool gl = h < NH;
+    // K and V rows are read once: evicted first, so that the verify logits written meanwhile
+    // are still in L2 when the Top-K pass reads them
+    const uint64_t kv_policy = l2_evict_first_policy();
     for (int rb = 0;; rb = rb + 1 == kRowLists ? 0 : rb + 1) {
         ok = mbar_wait(&c.rfull[rb], (fph >> rb) & 1, c.abort, c.err);
         if (!ok) break;
@@ -363,8 +383,8 @@ __device__ void loader(const AttnParams &p, const Ctx &c, int lane, int li) {
                 if (gl) {
                     char *dst = c.smem + S::off_stage + stage * S::STAGE + kv * S::ROWS + h * (kTileKeys * 128) +
                                 (RW * li + 4 * rgl) * 128;
-                    tma_gather4(dst, kv ? (const void *)&p.tmap_v : (const void *)&p.tmap_k, 64 * h, rr[0], rr[1], rr[2],
-                                rr[3], &c.full[stage]);
+                    tma_gather4_hint(dst, kv ? (const void *)&p.tmap_v : (const void *)&p.tmap_k, 64 * h, rr[0], rr[1],
+                                     rr[2], rr[3], &c.full[stage], kv_policy);
                 }
             }
             if (t == 0) {  // query rows into their operand slots (core-matrix layout), shared by the loaders
