@@ -357,7 +357,9 @@ def run_gpu(args):
     h_in = {n: getattr(g, n).cpu().pin_memory() for n in IN}
     h_out = [{n: torch.empty_like(getattr(g, n), device="cpu").pin_memory() for n in OUT} for _ in range(2)]
     d_in = [{n: getattr(g, n) for n in IN}, {n: torch.empty_like(getattr(g, n)) for n in IN}]
-    d_out = [{n: getattr(g, n) for n in OUT}, {n: torch.empty_like(getattr(g, n)) for n in OUT}]
+    # the second output set starts as a copy of the first: entries a step leaves untouched (lists
+    # past their count, all of them when there is no verify request) then agree as well
+    d_out = [{n: getattr(g, n) for n in OUT}, {n: getattr(g, n).clone() for n in OUT}]
     h2d = sum(t.numel() * t.element_size() for t in h_in.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
     copy = torch.cuda.Stream()
