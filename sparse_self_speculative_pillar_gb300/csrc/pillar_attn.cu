@@ -123,9 +123,11 @@ struct Smem {
     static constexpr int off_pend = off_meta + kMaxStages * (int)sizeof(StageMeta);
     static constexpr int off_bar = off_pend + kSBuf * 16;
     // full[8], empty[8], qempty[2], rfull[4], rempty[4], s_full[4], s_free[4], p_full[4], o_free[2], cexit, drain
-    static constexpr int NBAR = 2 * kMaxStages + 2 + 2 * kRowLists + 3 * kSBuf + 2 + 2;
+    static constexpr int NBAR = 2 * kMaxStages + 2 + 2 * kRowLists + 3 * kSBuf + 2 + 2 + 2 + 4 * kEpiWarps;
     static constexpr int off_misc = off_bar + NBAR * 8;
-    static constexpr int off_stage = (off_misc + 16 + 1023) / 1024 * 1024;
+    static constexpr int off_epi = off_misc + 16;  // per (epilogue warp, slot): EpiRec + 32 float2
+    static constexpr int EPI_BYTES = kEpiWarps * 2 * (32 + 32 * 8);
+    static constexpr int off_stage = (off_epi + EPI_BYTES + 1023) / 1024 * 1024;
     static constexpr int NSTAGE = (kSmemBudget - off_stage) / STAGE < kMaxStages ? (kSmemBudget - off_stage) / STAGE
                                                                                  : kMaxStages;
     static constexpr int used = off_stage + NSTAGE * STAGE;
@@ -137,6 +139,15 @@ static_assert(Smem<128>::total <= kSmemBudget && Smem<64>::total <= kSmemBudget,
 static_assert(Smem<128>::tO + 2 * 128 <= kTmemCols, "tensor memory budget");
 static_assert(sizeof(StageMeta) % 16 == 0 && sizeof(ItemInfo) == 64, "record layout");
 
+// An item whose O rows an epilogue warp is to write (handed over by the
+// consumer warp of the same quadrant through a two-slot mailbox).
+struct EpiRec {
+    int mode, g, q_off, nsplit, rec, qb;
+    int stop;  // no more items
+    int pad;
+};
+static_assert(sizeof(EpiRec) == 32, "epilogue record");
+
 struct Ctx {
     char *smem;
     StageMeta *meta;
@@ -144,6 +155,10 @@ struct Ctx {
     int *rowlist;  // [kRowLists][kMaxChunk]
     uint64_t *full, *empty, *qempty, *rfull, *rempty;
     uint64_t *s_full, *s_free, *p_full, *o_free, *cexit, *drain;
+    uint64_t *o_done;                // [2]: an item's last P V has completed (per O buffer)
+    uint64_t *epi_full, *epi_empty;  // [kEpiWarps * 2]: mailbox slots
+    EpiRec *epi;                     // [kEpiWarps * 2]
+    float2 *epi_inv;                 // [kEpiWarps * 2][32]: 1/l of each thread's two rows
     int4 *pend;  // [kSBuf] tiles between their S and P V MMAs (MMA thread only)
     volatile int *abort;
     uint32_t *tmem_slot;
@@ -170,6 +185,11 @@ __device__ __forceinline__ Ctx make_ctx(char *smem, const AttnParams &p) {
     c.o_free = c.p_full + kSBuf;
     c.cexit = c.o_free + 2;
     c.drain = c.cexit + 1;
+    c.o_done = c.drain + 1;
+    c.epi_full = c.o_done + 2;
+    c.epi_empty = c.epi_full + 2 * kEpiWarps;
+    c.epi = reinterpret_cast<EpiRec *>(smem + S::off_epi);
+    c.epi_inv = reinterpret_cast<float2 *>(smem + S::off_epi + 2 * kEpiWarps * 32);
     c.pend = reinterpret_cast<int4 *>(smem + S::off_pend);
     c.abort = reinterpret_cast<volatile int *>(smem + S::off_misc);
     c.tmem_slot = reinterpret_cast<uint32_t *>(smem + S::off_misc + 4);
@@ -503,6 +523,7 @@ __device__ void mma_issuer(const AttnParams &p, const Ctx &c, uint32_t tbase) {
                 umma_commit(&c.s_free[sb]);      // S/P buffer free, and the O of this tile final
                 umma_commit(&c.empty[e_stage]);  // K and V rows consumed
                 if (e_flags & kLast) {
+                    umma_commit(&c.o_done[e_qb]);  // the item's O is final: its epilogue may read it
                     started = false;
                     if (e_qb) ++ocount1; else ++ocount0;
                 }
@@ -542,7 +563,22 @@ struct CState {
     uint32_t phase;
     uint32_t vt;      // tiles this CTA has processed (selects S buffers and barrier parities)
     uint32_t tbase;   // TMEM base address
+    uint32_t items;   // items handed to the epilogue warp (their mailbox slot alternates)
 };
+
+// Hands the next mailbox slot of this warp's quadrant to its epilogue warp
+// (waiting, bounded, for the slot to have been taken two records back).
+__device__ __forceinline__ bool post_epilogue(const Ctx &c, int warp, int lane, CState &cs, const EpiRec &e, float2 inv) {
+    const int slot = warp * 2 + (int)(cs.items & 1);
+    const uint32_t use = cs.items >> 1;  // earlier uses of this slot
+    if (!mbar_wait(&c.epi_empty[slot], (use & 1) ^ 1, c.abort, c.err)) return false;
+    if (lane == 0) c.epi[slot] = e;
+    c.epi_inv[slot * 32 + lane] = inv;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c.epi_full[slot]);
+    ++cs.items;
+    return true;
+}
 
 constexpr float kRescaleLog2 = 8.f;  // O is rescaled once a row maximum has grown by more than 2^8
 
@@ -792,19 +828,69 @@ __device__ bool attn_item(const AttnParams &p, const Ctx &c, int warp, int lane,
                 p.part_lse[(size_t)in.rec + r.row] = lse;
         }
     }
-    if (!mbar_wait(&c.s_free[last_vt % kSBuf], (last_vt / kSBuf) & 1, c.abort, c.err)) return false;
-    tc_fence_after();
+    // the O rows are written by the epilogue warp of this quadrant once the item's last P V has
+    // completed; this warp goes on with the next item
+    (void)last_vt;
+    EpiRec e;
+    e.mode = in.mode;
+    e.g = in.g;
+    e.q_off = in.q_off;
+    e.nsplit = in.nsplit;
+    e.rec = in.rec;
+    e.qb = qb;
+    e.stop = 0;
+    e.pad = 0;
+    return post_epilogue(c, warp, lane, cs, e, make_float2(inva, invb));
+}
+
+// The epilogue warp of quadrant q: for each item of the consumer warp of its
+// quadrant, in order, wait until the item's last P V has completed, read its
+// O columns, normalise, write the rows (or the partial record of a split
+// item) and release the columns.
+template <int D>
+__device__ void epilogue_warp(const AttnParams &p, const Ctx &c, int q, int lane, uint32_t tbase) {
+    using S = Smem<D>;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;  // lanes 0-15 of quadrant q (M = 64)
+    const int cq = 2 * (lane & 3);
+    uint32_t odone = 0;  // bit b: parity of O buffer b's next completion
+    for (uint32_t n = 0;; ++n) {
+        const int slot = q * 2 + (int)(n & 1);
+        if (!mbar_wait(&c.epi_full[slot], (n >> 1) & 1, c.abort, c.err)) break;
+        const EpiRec e = c.epi[slot];
+        const float2 inv = c.epi_inv[slot * 32 + lane];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.epi_empty[slot]);  // the record is copied: the slot may be reused
+        if (e.stop) break;
+        if (!mbar_wait(&c.o_done[e.qb], (odone >> e.qb) & 1, c.abort, c.err)) break;
+        odone ^= 1u << e.qb;
+        tc_fence_after();
+        ItemInfo in;
+        in.mode = e.mode;
+        in.g = e.g;
+        in.q_off = e.q_off;
+        in.nsplit = e.nsplit;
+        in.rec = e.rec;
+        in.L = 0;  // (row limits and logit offsets are not used here)
+        in.logit_off = 0;
+        const bool verify = e.mode == 1;
+        const VRow ra = item_row(p, in, verify, q, lane >> 2);
+        const VRow rb = item_row(p, in, verify, q, 8 + (lane >> 2));
+        const bool have_b = (verify ? p.RQ : p.RQd) > 8;
+        const uint32_t tO = tbase + S::tO + (uint32_t)e.qb * D;
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 64) {
-        float ov[32];
-        tmem_ld16x256b_x8(tO + lane_base + c0, ov);  // warp-collective: every lane loads
-        row_output<D, 0>(p, in, ra, ov, c0, cq, inva);
-        if (have_b) row_output<D, 2>(p, in, rb, ov, c0, cq, invb);
+        for (int c0 = 0; c0 < D; c0 += 64) {
+            float ov[32];
+            tmem_ld16x256b_x8(tO + lane_base + c0, ov);  // warp-collective: every lane loads
+            row_output<D, 0>(p, in, ra, ov, c0, cq, inv.x);
+            if (have_b) row_output<D, 2>(p, in, rb, ov, c0, cq, inv.y);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.o_free[e.qb]);
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&c.o_free[qb]);
-    return true;
+    if (lane == 0) mbar_arrive(c.cexit);
 }
 
 template <int D>
@@ -814,18 +900,32 @@ __device__ void consumer(const AttnParams &p, const Ctx &c, int warp, int lane, 
     cs.phase = 0;
     cs.vt = 0;
     cs.tbase = tbase;
+    cs.items = 0;
     for (;;) {
         if (!mbar_wait(&c.full[cs.stage], cs.phase, c.abort, c.err)) break;
         const StageMeta m = c.meta[cs.stage];
         if (m.flags & kStop) break;
         if (!attn_item<D>(p, c, warp, lane, cs, m)) break;
     }
+    EpiRec stop = {};
+    stop.stop = 1;
+    post_epilogue(c, warp, lane, cs, stop, make_float2(0.f, 0.f));  // (returns at once on an abort)
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(c.cexit);
 }
 
 // ============================================================== kernel
+
+// Per-warp-group register reallocation (every warp of the group executes it).
+template <uint32_t R>
+__device__ __forceinline__ void regs_increase() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <uint32_t R>
+__device__ __forceinline__ void regs_decrease() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) unified_attn_kernel(const __grid_constant__ AttnParams p) {
@@ -851,8 +951,13 @@ __global__ void __launch_bounds__(kThreads, 1) unified_attn_kernel(const __grid_
             mbar_init(&c.s_free[i], 1);
             mbar_init(&c.p_full[i], kConsumerWarps);
         }
-        mbar_init(c.cexit, kConsumerWarps + 1);
+        mbar_init(c.cexit, kConsumerWarps + 1 + kEpiWarps);
         mbar_init(c.drain, 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&c.o_done[i], 1);
+        for (int i = 0; i < 2 * kEpiWarps; ++i) {
+            mbar_init(&c.epi_full[i], 1);
+            mbar_init(&c.epi_empty[i], 1);
+        }
         *c.abort = 0;
         mbar_init_fence();
     }
@@ -864,19 +969,31 @@ __global__ void __launch_bounds__(kThreads, 1) unified_attn_kernel(const __grid_
     // Everything above is private to the CTA; the plan's output is read only from here on.
     pdl_wait_prerequisites();
     pdl_launch_dependents();  // the merge kernel waits for this kernel's completion itself
-    if (warp < kConsumerWarps) {
+    // Registers move to the softmax warps: the CTA is launched with 128 per thread; the
+    // other three warp groups drop to 80 and the softmax group rises to 232
+    // (4*128*128 = 65536 >= 128*232 + 3*128*80 = 60416).
+    const int wg = warp >> 2;
+    if (wg == 0) {
+        regs_increase<232>();
         consumer<D>(p, c, warp, lane, tbase);
-    } else if (warp < kConsumerWarps + kLoaderWarps) {
+    } else if (wg == 1) {
+        regs_decrease<80>();
         loader<D>(p, c, lane, warp - kConsumerWarps);
-    } else if (warp == kConsumerWarps + kLoaderWarps) {
-        resolver(p, c, lane);
-    } else {
-        if (lane == 0) {
-            mma_issuer<D>(p, c, tbase);
-            tc_fence_before();
-            mbar_arrive(c.cexit);
+    } else if (wg == 2) {
+        regs_decrease<80>();
+        if (warp == 8) {
+            resolver(p, c, lane);
+        } else if (warp == 9) {
+            if (lane == 0) {
+                mma_issuer<D>(p, c, tbase);
+                tc_fence_before();
+                mbar_arrive(c.cexit);
+            }
+            __syncwarp();
         }
-        __syncwarp();
+    } else {
+        regs_decrease<80>();
+        epilogue_warp<D>(p, c, warp - 12, lane, tbase);
     }
     if (warp == 0) {  // the consumers and the MMA thread are done with the tensor memory (bounded wait), then free it
         drain_wait(c.cexit, 0);

@@ -13,7 +13,9 @@ namespace pillar {
 constexpr int kTileKeys = 64;          // keys staged per pipeline stage
 constexpr int kConsumerWarps = 4;      // compute warps per CTA (one per TMEM lane quadrant)
 constexpr int kLoaderWarps = 4;        // gather warps per CTA (each fetches 64 / kLoaderWarps rows of a tile)
-constexpr int kThreads = (kConsumerWarps + kLoaderWarps + 2) * 32;  // + a resolver and an MMA-issuing warp
+constexpr int kEpiWarps = 4;           // O-epilogue warps (one per TMEM lane quadrant)
+// four warp groups: consumers | loaders | resolver, MMA issuer and two spare warps | epilogue warps
+constexpr int kThreads = 16 * 32;
 constexpr int kMaxRows = 64;           // (k+1)*G bound of a verify tile
 constexpr int kMaxG = 8;               // query heads per KV head
 constexpr int kDefaultVerifyChunk = 1024;
