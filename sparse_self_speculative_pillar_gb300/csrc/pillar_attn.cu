@@ -15,7 +15,8 @@
 //
 // GB300 design: a persistent grid of one CTA per SM (the CTA owns the SM's
 // 512 tensor-memory columns and a ring of up to eight 64-key K/V stages in
-// shared memory), ten warps per CTA:
+// shared memory), sixteen warps per CTA in four groups (registers move to
+// the softmax group with setmaxnreg):
 //   * resolver warp: pops work items from a global atomic counter, reads the
 //     item's records and translates its positions into pool slots (list ->
 //     slot, many independent loads per lane) into a ring of four row lists,
@@ -44,6 +45,10 @@
 //     their own (alternating between items) and their O
 //     accumulators sit in separate TMEM columns, so an item's epilogue
 //     overlaps the next item's MMAs;
+//   * four epilogue warps, one per quadrant: the softmax warps hand each
+//     finished item over (a two-slot shared-memory mailbox per quadrant);
+//     once the item's last P V has completed, the epilogue warp reads its O
+//     columns, normalises, writes the rows and releases the columns;
 //   * a (request, KV head) split over several items (long contexts, long
 //     critical lists) writes normalised partials (o, lse) per item, combined
 //     afterwards by merge_kernel, a flat bandwidth pass:
