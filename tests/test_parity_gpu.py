@@ -298,3 +298,40 @@ def test_topk_long_rows_and_wide_ties(L, K, n_tied):
     if n_tied >= K:  # every kept position is one of the tied columns, the lowest ones
         for g in range(Hkv):
             np.testing.assert_array_equal(ni[0, g, :K], cols[:K])
+
+
+def _random_recipe(seed):
+    """A random shape and mix: head dim, GQA group, draft count k with
+    (k+1)*G <= 64 rows, a few requests of each phase, short and ragged
+    contexts, a random critical fraction and random work-item sizes."""
+    rng = np.random.default_rng(seed)
+    D = int(rng.choice([64, 128]))
+    Hkv = int(rng.integers(1, 4))
+    G = int(rng.integers(1, 9))
+    k = int(rng.integers(1, min(15, 64 // G - 1) + 1))
+    lo = int(rng.integers(k + 17, k + 300))
+    hi = int(rng.integers(lo, lo + 1500))
+    s_num, s_den = [(1, 20), (1, 8), (1, 3)][int(rng.integers(0, 3))]
+    rec = W.Recipe(f"random{seed}", B=int(rng.integers(k + 2, 2 * (k + 1) + 4)), Hq=G * Hkv, Hkv=Hkv, D=D, k=k,
+                   s_num=s_num, s_den=s_den, lengths=("uniform", lo, hi),
+                   pillar_frac=("uniform", 0.01, 0.1), seed=0x5EED1000 + seed)
+    chunks = [64, 128, 192, 512, 1024]
+    return rec, int(rng.choice(chunks)), int(rng.choice(chunks))
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes_and_item_sizes(seed):
+    """Random shapes, mixes and work-item sizes: every attention output element
+    against the oracle, then the Top-K of the step against the oracle's dump."""
+    rec, vchunk, dchunk = _random_recipe(seed)
+    w = W.generate(rec)
+    g = Gpu(w, verify_chunk=vchunk, draft_chunk=dchunk)
+    g.attn()
+    g.topk()
+    assert g.attn_flags() == 0 and g.topk_flags() == 0
+    res, ref, _ = _check(w, g)
+    if w.V:
+        t = oracle.topk_select(Hq=w.Hq, Hkv=w.Hkv, k=w.k, row_lo=1, row_hi=w.k + 1, logits=ref.logits,
+                               lse=oracle.verify_lse_of(ref, w.req_mode, w.k, w.Hq), L=w.verify_len, K=w.topk_K,
+                               max_topk=g.shape.max_topk)
+        compare_topk(res["next_idx"], res["next_cnt"], t, w.verify_len, w.topk_K, w.Hkv)
