@@ -275,6 +275,47 @@ def whole_job_us(max_elapsed_ms, steps, world):
 
 # --------------------------------------------------------------------------- GPU arm
 
+def fusion_ablation(g, P, stream, n):
+    """The attention call under the unified schedule and under the two
+    schedules it replaces ("SparseSpec-MLSys26", Unified batch scheduler +
+    fused attention kernel: a sequential pair of launches, and a joint batch
+    without per-mode dispatch), each timed over n calls on the launching
+    stream.  Every schedule writes the same outputs; `*_same_out` says whether
+    the out tensor came back bit for bit equal to the unified pass's."""
+    import torch
+    plans = (("unified", (P.SCHEDULE_UNIFIED,)),
+             ("sequential", (P.SCHEDULE_DRAFT_ONLY, P.SCHEDULE_VERIFY_ONLY)),
+             ("uniform_rows", (P.SCHEDULE_UNIFORM_ROWS,)))
+
+    def run(scheds):
+        for sch in scheds:
+            g.shape.schedule = sch
+            g.attn(stream)
+        g.shape.schedule = P.SCHEDULE_UNIFIED
+
+    run(plans[0][1])
+    torch.cuda.synchronize()
+    ref = g.out.clone()
+    res = {"calls": n}
+    for name, scheds in plans:
+        for _ in range(3):
+            run(scheds)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            run(scheds)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name + "_attn_us"] = e0.elapsed_time(e1) * 1e3 / n
+        res[name + "_same_out"] = bool(torch.equal(g.out, ref))
+        res[name + "_flags"] = g.attn_flags()
+    run(plans[0][1])
+    torch.cuda.synchronize()
+    for name, _ in plans[1:]:
+        res[name + "_vs_unified"] = res[name + "_attn_us"] / res["unified_attn_us"]
+    return res
+
+
 def run_gpu(args):
     import torch
     import sparse_self_speculative_pillar_gb300 as P
@@ -421,6 +462,7 @@ def run_gpu(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, "cuda")
     e2e_us = whole_job_us(e2e_ms, e2e_steps, world)
     flags = g.attn_flags() | g.topk_flags()
+    ablation = fusion_ablation(g, P, stream, max(10, min(args.steps, 500)))
 
     if rank != 0:
         if world > 1:
@@ -462,6 +504,7 @@ def run_gpu(args):
                             "double-buffered device sets, transfers on a copy stream overlapping the previous "
                             "or next step's compute",
                 "serial_value": serial_us},
+        "fusion_ablation": ablation,
         "gpu_launches": 5 * args.steps,
         "breakdown_steps": nb,
         "clocks": clk,

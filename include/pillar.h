@@ -81,8 +81,33 @@ typedef struct pillar_shape {
     int32_t draft_chunk;   /* listed keys per draft work item (multiple of 64, <= 1024; 0 = 1024) */
     int64_t num_slots;     /* rows of k_pool / v_pool */
     float sm_scale;        /* logit scale; 0 means 1/sqrt(D) */
-    int32_t reserved;      /* must be 0 */
+    int32_t schedule;      /* PILLAR_SCHEDULE_* (0: the unified pass) */
 } pillar_shape_t;
+
+/*
+ * Schedules of pillar_attn_unified.  The unified pass is the method's design
+ * ("SparseSpec-MLSys26", Unified batch scheduler + fused attention kernel:
+ * one persistent kernel serves draft and verify requests of one batch).  The
+ * other schedules exist to measure it against the two alternatives that
+ * section compares it with; all of them compute the same outputs.
+ *   UNIFIED       draft and verify requests in one persistent pass.
+ *   DRAFT_ONLY    the draft requests only; the outputs of verify requests
+ *                 (their out rows, logits and LSEs) are left untouched.
+ *   VERIFY_ONLY   the verify requests only; draft outputs left untouched.  A
+ *                 DRAFT_ONLY call followed by a VERIFY_ONLY call on the same
+ *                 buffers is the sequential two-kernel schedule; it writes
+ *                 the same values as one UNIFIED call.
+ *   UNIFORM_ROWS  one pass in which a draft item takes the verify item's row
+ *                 layout (its G rows as the first G of the (k+1)*G row slots,
+ *                 the slots of one TMEM lane quadrant) instead of its own
+ *                 spread of the G rows over the four quadrants: a joint batch
+ *                 without per-mode dispatch.
+ * The device error word is cleared by every call; it reports that call only.
+ */
+#define PILLAR_SCHEDULE_UNIFIED 0
+#define PILLAR_SCHEDULE_DRAFT_ONLY 1
+#define PILLAR_SCHEDULE_VERIFY_ONLY 2
+#define PILLAR_SCHEDULE_UNIFORM_ROWS 3
 
 /*
  * pillar_attn_workspace_bytes -- bytes of workspace pillar_attn_unified

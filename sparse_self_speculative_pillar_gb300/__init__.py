@@ -29,9 +29,12 @@ __all__ = [
     "pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_topk_workspace_bytes",
     "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string",
     "FLAG_INDEX", "FLAG_SLOT", "FLAG_REQUEST", "FLAG_COUNT", "FLAG_TIMEOUT", "FLAG_TOPK",
+    "SCHEDULE_UNIFIED", "SCHEDULE_DRAFT_ONLY", "SCHEDULE_VERIFY_ONLY", "SCHEDULE_UNIFORM_ROWS",
 ]
 
 FLAG_INDEX, FLAG_SLOT, FLAG_REQUEST, FLAG_COUNT, FLAG_TIMEOUT, FLAG_TOPK = 1, 2, 4, 8, 16, 32
+# values of PillarShape.schedule (PILLAR_SCHEDULE_* in the header)
+SCHEDULE_UNIFIED, SCHEDULE_DRAFT_ONLY, SCHEDULE_VERIFY_ONLY, SCHEDULE_UNIFORM_ROWS = 0, 1, 2, 3
 EXPORTED = ("pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_topk_workspace_bytes",
             "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string")
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024 + 256
@@ -44,16 +47,16 @@ class PillarShape(ctypes.Structure):
         ("k", ctypes.c_int32), ("max_sparse", ctypes.c_int32), ("max_len", ctypes.c_int32),
         ("row_lo", ctypes.c_int32), ("row_hi", ctypes.c_int32), ("max_topk", ctypes.c_int32),
         ("verify_chunk", ctypes.c_int32), ("draft_chunk", ctypes.c_int32), ("num_slots", ctypes.c_int64),
-        ("sm_scale", ctypes.c_float), ("reserved", ctypes.c_int32),
+        ("sm_scale", ctypes.c_float), ("schedule", ctypes.c_int32),
     ]
 
 
 def make_shape(*, B, Hq, Hkv, D, k, max_sparse, max_len, num_slots, max_topk=1, row_lo=1, row_hi=None,
-               verify_chunk=0, draft_chunk=0, sm_scale=0.0) -> PillarShape:
+               verify_chunk=0, draft_chunk=0, sm_scale=0.0, schedule=0) -> PillarShape:
     return PillarShape(B=B, Hq=Hq, Hkv=Hkv, D=D, k=k, max_sparse=max_sparse, max_len=max_len,
                        row_lo=row_lo, row_hi=(k + 1) if row_hi is None else row_hi, max_topk=max(1, max_topk),
                        verify_chunk=verify_chunk, draft_chunk=draft_chunk, num_slots=num_slots,
-                       sm_scale=sm_scale, reserved=0)
+                       sm_scale=sm_scale, schedule=schedule)
 
 
 class PillarError(RuntimeError):

@@ -25,7 +25,7 @@ int check_shape(const pillar_shape_t *s) {
     // the pools are addressed as num_slots * Hkv rows with 32-bit row coordinates
     if (s->Hkv > 0 && s->num_slots > 0x7fffffffll / s->Hkv) return PILLAR_ERR_ARG;
     if (s->row_lo < 0 || s->row_hi > s->k + 1 || s->row_lo >= s->row_hi) return PILLAR_ERR_ARG;
-    if (s->reserved != 0) return PILLAR_ERR_ARG;
+    if (s->schedule < PILLAR_SCHEDULE_UNIFIED || s->schedule > PILLAR_SCHEDULE_UNIFORM_ROWS) return PILLAR_ERR_ARG;
     if (!(s->sm_scale >= 0.f) || std::isinf(s->sm_scale)) return PILLAR_ERR_ARG;
     for (int c : {s->verify_chunk, s->draft_chunk})
         if (c != 0 && (c < kTileKeys || c > kMaxChunk || c % kTileKeys != 0)) return PILLAR_ERR_ARG;
@@ -96,6 +96,7 @@ int pillar_attn_unified(const pillar_shape_t *shape, const uint16_t *q, const ui
     pa.max_len = s.max_len;
     pa.vchunk = verify_chunk_of(s);
     pa.dchunk = draft_chunk_of(s);
+    pa.schedule = s.schedule;
     if (launch_plan(pa, cs) != cudaSuccess) return PILLAR_ERR_CUDA;
 
     AttnArgs aa;
@@ -115,6 +116,7 @@ int pillar_attn_unified(const pillar_shape_t *shape, const uint16_t *q, const ui
     aa.D = s.D;
     aa.k = s.k;
     aa.max_sparse = s.max_sparse;
+    aa.schedule = s.schedule;
     aa.scale = s.sm_scale > 0.f ? s.sm_scale : 1.0f / std::sqrt((float)s.D);
     if (launch_attn(aa, nsm, cs) != cudaSuccess) return PILLAR_ERR_CUDA;
     return PILLAR_OK;

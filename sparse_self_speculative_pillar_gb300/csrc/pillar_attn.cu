@@ -1186,7 +1186,9 @@ cudaError_t launch_attn(const AttnArgs &a, int nsm, cudaStream_t st) {
     p.k = a.k;
     p.M = (a.k + 1) * p.G;
     p.RQ = (p.M + kConsumerWarps - 1) / kConsumerWarps;
-    p.RQd = (p.G + kConsumerWarps - 1) / kConsumerWarps;
+    // draft items spread their G rows over the four quadrants, except in the
+    // uniform-rows schedule, where they take the verify row layout
+    p.RQd = a.schedule == PILLAR_SCHEDULE_UNIFORM_ROWS ? p.RQ : (p.G + kConsumerWarps - 1) / kConsumerWarps;
     p.max_sparse = a.max_sparse;
     p.scale = a.scale;
     return a.D == 128 ? launch_unified_t<128>(p, nsm, st) : launch_unified_t<64>(p, nsm, st);

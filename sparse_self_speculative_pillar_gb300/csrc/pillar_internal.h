@@ -120,6 +120,7 @@ struct PlanArgs {
     char *ws;
     AttnLayout lay;
     int B, Hq, Hkv, k, max_sparse, max_len, vchunk, dchunk;
+    int schedule;  // PILLAR_SCHEDULE_*
 };
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t st);
 
@@ -132,6 +133,7 @@ struct AttnArgs {
     AttnLayout lay;
     long long num_slots;
     int Hq, Hkv, D, k, max_sparse;
+    int schedule;  // PILLAR_SCHEDULE_*
     float scale;
 };
 cudaError_t launch_attn(const AttnArgs &a, int grid, cudaStream_t st);

@@ -31,6 +31,7 @@ struct PlanParams {
     MergeUnit *merge_units;
     Item *items;
     int B, Hq, Hkv, k, max_sparse, max_len, vchunk, dchunk;
+    int schedule;  // PILLAR_SCHEDULE_*
 };
 
 constexpr int kScanN = 8;
@@ -101,8 +102,15 @@ __device__ __forceinline__ int chunking(int n, int chunk, int *ns) {
 }
 
 // Keys, split count and chunk size of a unit of a request with record r;
-// cnt is the unit's sparse_cnt entry (used by draft units only).
+// cnt is the unit's sparse_cnt entry (used by draft units only).  A request
+// that the schedule leaves out of this call has no items (ns = 0).
 __device__ __forceinline__ int unit_split(const PlanParams &p, const ReqInfo &r, int cnt, int *n, int *ns, int *bad) {
+    if ((p.schedule == PILLAR_SCHEDULE_DRAFT_ONLY && r.mode == 1) ||
+        (p.schedule == PILLAR_SCHEDULE_VERIFY_ONLY && r.mode == 0)) {
+        *n = 0;
+        *ns = 0;
+        return 0;
+    }
     if (r.mode == 1) {
         *n = r.len;
         return chunking(r.len, p.vchunk, ns);
@@ -292,6 +300,7 @@ cudaError_t launch_plan(const PlanArgs &a, cudaStream_t st) {
     p.max_len = a.max_len;
     p.vchunk = a.vchunk;
     p.dchunk = a.dchunk;
+    p.schedule = a.schedule;
     plan_kernel<<<1, kPlanThreads, 0, st>>>(p);
     return cudaGetLastError();
 }

@@ -103,6 +103,46 @@ def test_split_and_merge_matches_unsplit(vchunk, dchunk):
     _check(w, g)
 
 
+def test_schedules_write_the_unified_outputs():
+    """The sequential two-launch schedule (the draft requests, then the verify
+    requests) writes exactly the values of one unified pass, each launch
+    leaving the other mode's outputs untouched; the uniform-rows schedule
+    (draft items in the verify row layout) matches the oracle."""
+    import sparse_self_speculative_pillar_gb300 as P
+    w = W.generate(W.scaled("qwen3_8b", B=19, length_scale=0.05, seed_offset=6))
+    uni = Gpu(w, verify_chunk=128, draft_chunk=64)  # split units too
+    uni.attn()
+    assert uni.attn_flags() == 0
+    a = uni.host()
+    raw_a = uni.out.cpu().numpy()
+
+    g = Gpu(w, verify_chunk=128, draft_chunk=64, schedule=P.SCHEDULE_DRAFT_ONLY)
+    g.out.fill_(-1)  # an all-ones bf16 pattern (NaN) marks rows never written
+    g.attn()
+    assert g.attn_flags() == 0
+    raw = g.out.cpu().numpy()
+    rows = np.zeros(raw.shape[0], bool)  # query rows of draft requests
+    for b in range(w.B):
+        if w.req_mode[b] == 0:
+            rows[w.q_off[b]] = True
+    np.testing.assert_array_equal(raw[rows], raw_a[rows])
+    assert np.all(raw[~rows] == -1)
+    assert np.isnan(g.logits.cpu().numpy()).all() and np.isnan(g.lse.cpu().numpy()).all()
+
+    g.shape.schedule = P.SCHEDULE_VERIFY_ONLY
+    g.attn()
+    assert g.attn_flags() == 0
+    b2 = g.host()
+    np.testing.assert_array_equal(g.out.cpu().numpy(), raw_a)
+    np.testing.assert_array_equal(b2["logits"], a["logits"])
+    np.testing.assert_array_equal(b2["lse"], a["lse"])
+
+    u = Gpu(w, verify_chunk=128, draft_chunk=64, schedule=P.SCHEDULE_UNIFORM_ROWS)
+    u.attn()
+    assert u.attn_flags() == 0
+    _check(w, u)
+
+
 def test_repeated_calls_are_identical():
     w = W.generate(W.scaled("stress", B=15, length_scale=0.04, seed_offset=5))
     g = Gpu(w, verify_chunk=128)
