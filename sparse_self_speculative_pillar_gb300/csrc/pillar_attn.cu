@@ -19,8 +19,8 @@
 // the softmax group with setmaxnreg):
 //   * resolver warp: pops work items from a global atomic counter, reads the
 //     item's records and translates its positions into pool slots (list ->
-//     slot, many independent loads per lane) into a ring of four row lists,
-//     up to three items ahead of the loaders;
+//     slot, many independent loads per lane) into a ring of three row lists,
+//     up to two items ahead of the loaders;
 //   * four loader warps: gather the item's K/V rows into the stage ring with
 //     TMA tile::gather4 (four 256-byte page-size-1 rows per copy) in the
 //     swizzled layout the tensor cores read, completion counted in bytes on
@@ -107,7 +107,7 @@ struct StageMeta {
 };
 
 constexpr int kSBuf = 4;                  // S/P buffers in tensor memory
-constexpr int kRowLists = 4;              // resolved items in flight between the resolver and the loaders
+constexpr int kRowLists = 3;              // resolved items in flight between the resolver and the loaders
 constexpr int kMaxStages = 8;             // K/V stages in shared memory
 constexpr int kSmemBudget = 227 * 1024;   // dynamic shared memory of one CTA
 constexpr int kMinSmem = 120 * 1024;      // never two CTAs on one SM: each takes all 512 TMEM columns

@@ -18,9 +18,14 @@ constexpr int kEpiWarps = 4;           // O-epilogue warps (one per TMEM lane qu
 constexpr int kThreads = 16 * 32;
 constexpr int kMaxRows = 64;           // (k+1)*G bound of a verify tile
 constexpr int kMaxG = 8;               // query heads per KV head
+// Default verify item size: 1024 keys for contexts shorter than kLongContext
+// positions, 2048 from there on (fewer items and partial records where the
+// per-item cost weighs, enough items to balance the CTAs below).
 constexpr int kDefaultVerifyChunk = 1024;
+constexpr int kLongVerifyChunk = 2048;
+constexpr int kLongContext = 8192;
 constexpr int kDefaultDraftChunk = 1024;
-constexpr int kMaxChunk = 1024;        // item key bound (sizes the resolved row lists in shared memory)
+constexpr int kMaxChunk = 2048;        // item key bound (sizes the resolved row lists in shared memory)
 constexpr int kPlanThreads = 1024;
 constexpr unsigned long long kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
@@ -74,7 +79,8 @@ struct AttnLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-inline int verify_chunk_of(const pillar_shape_t &s) { return s.verify_chunk > 0 ? s.verify_chunk : kDefaultVerifyChunk; }
+// 0: the default, chosen per request by its context length (see kLongContext)
+inline int verify_chunk_of(const pillar_shape_t &s) { return s.verify_chunk > 0 ? s.verify_chunk : 0; }
 inline int draft_chunk_of(const pillar_shape_t &s) { return s.draft_chunk > 0 ? s.draft_chunk : kDefaultDraftChunk; }
 
 // Partials: an item of a (request, KV head) split over several items writes
@@ -84,7 +90,8 @@ inline AttnLayout attn_layout(const pillar_shape_t &s) {
     AttnLayout l{};
     const long long B = s.B, U = (long long)s.B * s.Hkv;
     const int G = s.Hq / s.Hkv;
-    const long long vc = verify_chunk_of(s), dc = draft_chunk_of(s);
+    // (the default verify chunk is bounded by its smaller size: the most items)
+    const long long vc = verify_chunk_of(s) > 0 ? verify_chunk_of(s) : kDefaultVerifyChunk, dc = draft_chunk_of(s);
     long long per_unit = (s.max_len + vc - 1) / vc;
     long long dsplit = (s.max_sparse + dc - 1) / dc;
     if (dsplit > per_unit) per_unit = dsplit;

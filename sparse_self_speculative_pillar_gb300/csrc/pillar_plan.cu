@@ -113,7 +113,8 @@ __device__ __forceinline__ int unit_split(const PlanParams &p, const ReqInfo &r,
     }
     if (r.mode == 1) {
         *n = r.len;
-        return chunking(r.len, p.vchunk, ns);
+        const int vc = p.vchunk > 0 ? p.vchunk : (r.len >= kLongContext ? kLongVerifyChunk : kDefaultVerifyChunk);
+        return chunking(r.len, vc, ns);
     }
     int c = r.mode == 0 ? cnt : 0;
     if (c < 0 || c > p.max_sparse) *bad |= PILLAR_FLAG_COUNT;

@@ -355,7 +355,7 @@ def _random_recipe(seed):
     rec = W.Recipe(f"random{seed}", B=int(rng.integers(k + 2, 2 * (k + 1) + 4)), Hq=G * Hkv, Hkv=Hkv, D=D, k=k,
                    s_num=s_num, s_den=s_den, lengths=("uniform", lo, hi),
                    pillar_frac=("uniform", 0.01, 0.1), seed=0x5EED1000 + seed)
-    chunks = [64, 128, 192, 512, 1024]
+    chunks = [0, 64, 128, 192, 512, 1024, 2048]  # 0: the default item sizes
     return rec, int(rng.choice(chunks)), int(rng.choice(chunks))
 
 
