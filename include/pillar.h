@@ -235,6 +235,48 @@ PILLAR_API int pillar_get_error(void *workspace, void *stream, int32_t *flags);
 /* pillar_status_string -- a static English description of a return code. */
 PILLAR_API const char *pillar_status_string(int status);
 
+/*
+ * Phase buckets of the unified batch (host side; "SparseSpec-MLSys26",
+ * Unified batch scheduler + fused attention kernel, load balancing).  Every
+ * request runs a cycle of k+1 steps: k draft steps (phases 1..k), then one
+ * verify step (phase 0).  A request in bucket c is in phase (c + t) mod (k+1)
+ * at step t, so the requests of one bucket verify together.  A new request
+ * joins the bucket with the fewest requests (ties to the lowest index), which
+ * keeps the verify requests of a step near B/(k+1) and the step's query rows
+ * near (2k+1)/(k+1)*B instead of alternating between B and (k+1)*B.
+ *
+ * The state is a plain caller-owned struct; nothing is allocated and no GPU
+ * is touched.  Every function returns PILLAR_OK or PILLAR_ERR_ARG (a null
+ * pointer, k outside [0, PILLAR_MAX_BUCKETS - 1], a bucket outside
+ * [0, k], retiring from an empty bucket, n < 0) and changes nothing on error.
+ */
+#define PILLAR_MAX_BUCKETS 64
+typedef struct pillar_buckets {
+    int32_t nbuckets;                    /* k + 1 */
+    int32_t count[PILLAR_MAX_BUCKETS];   /* requests in each bucket */
+} pillar_buckets_t;
+
+/* pillar_buckets_init -- k+1 empty buckets. */
+PILLAR_API int pillar_buckets_init(pillar_buckets_t *pb, int32_t k);
+
+/* pillar_buckets_admit -- places a new request: *bucket gets the least
+ * loaded bucket (the lowest index among equals), whose count grows by one. */
+PILLAR_API int pillar_buckets_admit(pillar_buckets_t *pb, int32_t *bucket);
+
+/* pillar_buckets_retire -- a request of `bucket` has finished. */
+PILLAR_API int pillar_buckets_retire(pillar_buckets_t *pb, int32_t bucket);
+
+/*
+ * pillar_buckets_step -- the inputs of step `step` for n requests whose
+ * buckets are bucket[0..n): req_mode[i] = 1 (verify) when the request's phase
+ * is 0, else 0 (draft), and phase[i] in [0, k] (either output may be null).
+ * *q_rows (nullable) gets the step's query rows, k+1 per verify request and
+ * one per draft request (the T_q of pillar_attn_unified).  All pointers are
+ * host memory.
+ */
+PILLAR_API int pillar_buckets_step(const pillar_buckets_t *pb, const int32_t *bucket, int32_t n, int64_t step,
+                                   int32_t *req_mode, int32_t *phase, int64_t *q_rows);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,6 +16,8 @@ Entry points (same names as the C ABI):
                      next_idx, next_cnt, workspace, stream=None)
   pillar_get_error(workspace, stream=None)
   pillar_status_string(status)
+  pillar_buckets_init(k), pillar_buckets_admit(pb), pillar_buckets_retire(pb, bucket),
+  pillar_buckets_step(pb, buckets, step)    (host-side phase buckets)
 """
 from __future__ import annotations
 
@@ -30,13 +32,16 @@ __all__ = [
     "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string",
     "FLAG_INDEX", "FLAG_SLOT", "FLAG_REQUEST", "FLAG_COUNT", "FLAG_TIMEOUT", "FLAG_TOPK",
     "SCHEDULE_UNIFIED", "SCHEDULE_DRAFT_ONLY", "SCHEDULE_VERIFY_ONLY", "SCHEDULE_UNIFORM_ROWS",
+    "PillarBuckets", "pillar_buckets_init", "pillar_buckets_admit", "pillar_buckets_retire", "pillar_buckets_step",
 ]
 
 FLAG_INDEX, FLAG_SLOT, FLAG_REQUEST, FLAG_COUNT, FLAG_TIMEOUT, FLAG_TOPK = 1, 2, 4, 8, 16, 32
 # values of PillarShape.schedule (PILLAR_SCHEDULE_* in the header)
 SCHEDULE_UNIFIED, SCHEDULE_DRAFT_ONLY, SCHEDULE_VERIFY_ONLY, SCHEDULE_UNIFORM_ROWS = 0, 1, 2, 3
 EXPORTED = ("pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_topk_workspace_bytes",
-            "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string")
+            "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string",
+            "pillar_buckets_init", "pillar_buckets_admit", "pillar_buckets_retire", "pillar_buckets_step")
+MAX_BUCKETS = 64  # PILLAR_MAX_BUCKETS
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024 + 256
 
 
@@ -57,6 +62,11 @@ def make_shape(*, B, Hq, Hkv, D, k, max_sparse, max_len, num_slots, max_topk=1, 
                        row_lo=row_lo, row_hi=(k + 1) if row_hi is None else row_hi, max_topk=max(1, max_topk),
                        verify_chunk=verify_chunk, draft_chunk=draft_chunk, num_slots=num_slots,
                        sm_scale=sm_scale, schedule=schedule)
+
+
+class PillarBuckets(ctypes.Structure):
+    """pillar_buckets_t: the request count of each of the k+1 phase buckets."""
+    _fields_ = [("nbuckets", ctypes.c_int32), ("count", ctypes.c_int32 * MAX_BUCKETS)]
 
 
 class PillarError(RuntimeError):
@@ -99,6 +109,13 @@ def load():
     lib.pillar_topk_select_noalloc.argtypes = [SP, ctypes.c_int32] + [P] * 8 + [P]
     lib.pillar_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     lib.pillar_status_string.argtypes = [ctypes.c_int]
+    BP = ctypes.POINTER(PillarBuckets)
+    I32P = ctypes.POINTER(ctypes.c_int32)
+    lib.pillar_buckets_init.argtypes = [BP, ctypes.c_int32]
+    lib.pillar_buckets_admit.argtypes = [BP, I32P]
+    lib.pillar_buckets_retire.argtypes = [BP, ctypes.c_int32]
+    lib.pillar_buckets_step.argtypes = [BP, I32P, ctypes.c_int32, ctypes.c_int64, I32P, I32P,
+                                        ctypes.POINTER(ctypes.c_int64)]
     lib.pillar_status_string.restype = ctypes.c_char_p
     for n in EXPORTED:
         if n == "pillar_status_string":
@@ -201,3 +218,42 @@ def pillar_get_error(workspace, stream=None) -> int:
     if st not in (0, -4):
         raise PillarError("pillar_get_error", st)
     return int(flags.value)
+
+
+# --------------------------------------------------------------- phase buckets (host side)
+
+def pillar_buckets_init(k: int) -> PillarBuckets:
+    pb = PillarBuckets()
+    st = load().pillar_buckets_init(ctypes.byref(pb), int(k))
+    if st:
+        raise PillarError("pillar_buckets_init", st)
+    return pb
+
+
+def pillar_buckets_admit(pb: PillarBuckets) -> int:
+    """Bucket of a new request (the least loaded one, lowest index among equals)."""
+    b = ctypes.c_int32(-1)
+    st = load().pillar_buckets_admit(ctypes.byref(pb), ctypes.byref(b))
+    if st:
+        raise PillarError("pillar_buckets_admit", st)
+    return int(b.value)
+
+
+def pillar_buckets_retire(pb: PillarBuckets, bucket: int) -> None:
+    st = load().pillar_buckets_retire(ctypes.byref(pb), int(bucket))
+    if st:
+        raise PillarError("pillar_buckets_retire", st)
+
+
+def pillar_buckets_step(pb: PillarBuckets, buckets, step: int):
+    """(req_mode, phase, q_rows) of the requests with these buckets at `step`
+    (lists of ints and the step's query-row count)."""
+    n = len(buckets)
+    arr = (ctypes.c_int32 * max(1, n))(*buckets)
+    mode = (ctypes.c_int32 * max(1, n))()
+    phase = (ctypes.c_int32 * max(1, n))()
+    rows = ctypes.c_int64(0)
+    st = load().pillar_buckets_step(ctypes.byref(pb), arr, n, int(step), mode, phase, ctypes.byref(rows))
+    if st:
+        raise PillarError("pillar_buckets_step", st)
+    return list(mode)[:n], list(phase)[:n], int(rows.value)

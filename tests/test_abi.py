@@ -36,6 +36,11 @@ def test_shape_struct_matches_header_layout():
     # 12 int32, then int64 (8-aligned at 48), float, int32 -> 64 bytes
     assert ctypes.sizeof(P.PillarShape) == 64
     assert P.PillarShape.num_slots.offset == 48
+    assert P.PillarShape.schedule.offset == 60
+    # pillar_buckets_t: int32 nbuckets, then PILLAR_MAX_BUCKETS int32 counts
+    src = open(os.path.join(ROOT, "include", "pillar.h")).read()
+    assert int(re.search(r"#define PILLAR_MAX_BUCKETS (\d+)", src).group(1)) == P.MAX_BUCKETS
+    assert ctypes.sizeof(P.PillarBuckets) == 4 * (1 + P.MAX_BUCKETS)
 
 
 def _shape(**kw):
