@@ -236,6 +236,29 @@ PILLAR_API int pillar_get_error(void *workspace, void *stream, int32_t *flags);
 PILLAR_API const char *pillar_status_string(int status);
 
 /*
+ * pillar_kv_append -- writes n new tokens' K and V rows into their page-size-1
+ * slots (the step before the unified pass: the token a draft step appends or
+ * the k+1 tokens of a verify step go to whatever slots the caller's allocator
+ * handed out; "SparseSpec-MLSys26", Unified batch scheduler + fused attention
+ * kernel: page size 1):
+ *   k_pool[slots[i], h, :] = k_new[i, h, :],  v_pool[slots[i], h, :] = v_new[i, h, :]
+ * for i < n and h < Hkv.  Only shape->Hkv, D and num_slots are used.
+ *   k_new, v_new   [n, Hkv, D] bf16, device memory, 16-byte aligned
+ *   slots          [n] int32, device memory; distinct (for a repeated slot one
+ *                  of the writes wins)
+ *   k_pool, v_pool [num_slots, Hkv, D] bf16, device memory, 16-byte aligned
+ *   device_flags   device int32 or null: PILLAR_FLAG_SLOT is or-ed into it
+ *                  when a slot lies outside [0, num_slots); that token is
+ *                  skipped and no other row is touched
+ * Asynchronous on `stream`; allocates nothing.  Returns PILLAR_OK,
+ * PILLAR_ERR_ARG (bad shape, n < 0, a null or misaligned pointer) or
+ * PILLAR_ERR_CUDA.
+ */
+PILLAR_API int pillar_kv_append(const pillar_shape_t *shape, const uint16_t *k_new, const uint16_t *v_new,
+                                const int32_t *slots, int32_t n, uint16_t *k_pool, uint16_t *v_pool,
+                                int32_t *device_flags, void *stream);
+
+/*
  * Phase buckets of the unified batch (host side; "SparseSpec-MLSys26",
  * Unified batch scheduler + fused attention kernel, load balancing).  Every
  * request runs a cycle of k+1 steps: k draft steps (phases 1..k), then one

@@ -16,6 +16,7 @@ Entry points (same names as the C ABI):
                      next_idx, next_cnt, workspace, stream=None)
   pillar_get_error(workspace, stream=None)
   pillar_status_string(status)
+  pillar_kv_append(shape, k_new, v_new, slots, k_pool, v_pool, device_flags=None, stream=None)
   pillar_buckets_init(k), pillar_buckets_admit(pb), pillar_buckets_retire(pb, bucket),
   pillar_buckets_step(pb, buckets, step)    (host-side phase buckets)
 """
@@ -32,7 +33,7 @@ __all__ = [
     "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string",
     "FLAG_INDEX", "FLAG_SLOT", "FLAG_REQUEST", "FLAG_COUNT", "FLAG_TIMEOUT", "FLAG_TOPK",
     "SCHEDULE_UNIFIED", "SCHEDULE_DRAFT_ONLY", "SCHEDULE_VERIFY_ONLY", "SCHEDULE_UNIFORM_ROWS",
-    "PillarBuckets", "pillar_buckets_init", "pillar_buckets_admit", "pillar_buckets_retire", "pillar_buckets_step",
+    "pillar_kv_append", "PillarBuckets", "pillar_buckets_init", "pillar_buckets_admit", "pillar_buckets_retire", "pillar_buckets_step",
 ]
 
 FLAG_INDEX, FLAG_SLOT, FLAG_REQUEST, FLAG_COUNT, FLAG_TIMEOUT, FLAG_TOPK = 1, 2, 4, 8, 16, 32
@@ -40,7 +41,8 @@ FLAG_INDEX, FLAG_SLOT, FLAG_REQUEST, FLAG_COUNT, FLAG_TIMEOUT, FLAG_TOPK = 1, 2,
 SCHEDULE_UNIFIED, SCHEDULE_DRAFT_ONLY, SCHEDULE_VERIFY_ONLY, SCHEDULE_UNIFORM_ROWS = 0, 1, 2, 3
 EXPORTED = ("pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_topk_workspace_bytes",
             "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string",
-            "pillar_buckets_init", "pillar_buckets_admit", "pillar_buckets_retire", "pillar_buckets_step")
+            "pillar_kv_append", "pillar_buckets_init", "pillar_buckets_admit", "pillar_buckets_retire",
+            "pillar_buckets_step")
 MAX_BUCKETS = 64  # PILLAR_MAX_BUCKETS
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024 + 256
 
@@ -109,6 +111,7 @@ def load():
     lib.pillar_topk_select_noalloc.argtypes = [SP, ctypes.c_int32] + [P] * 8 + [P]
     lib.pillar_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
     lib.pillar_status_string.argtypes = [ctypes.c_int]
+    lib.pillar_kv_append.argtypes = [SP, P, P, P, ctypes.c_int32, P, P, P, P]
     BP = ctypes.POINTER(PillarBuckets)
     I32P = ctypes.POINTER(ctypes.c_int32)
     lib.pillar_buckets_init.argtypes = [BP, ctypes.c_int32]
@@ -218,6 +221,18 @@ def pillar_get_error(workspace, stream=None) -> int:
     if st not in (0, -4):
         raise PillarError("pillar_get_error", st)
     return int(flags.value)
+
+
+def pillar_kv_append(shape, k_new, v_new, slots, k_pool, v_pool, device_flags=None, stream=None):
+    """Scatter n new tokens' K/V rows ([n, Hkv, D] bf16) into the pools at
+    slots[0..n); out-of-range slots are skipped and flagged in device_flags."""
+    n = int(slots.numel()) if not isinstance(slots, int) else None
+    if n is None:
+        raise ValueError("slots must be a tensor (its length is the token count)")
+    st = load().pillar_kv_append(ctypes.byref(shape), _ptr(k_new), _ptr(v_new), _ptr(slots), n, _ptr(k_pool),
+                                 _ptr(v_pool), _ptr(device_flags), _stream(stream))
+    if st:
+        raise PillarError("pillar_kv_append", st)
 
 
 # --------------------------------------------------------------- phase buckets (host side)

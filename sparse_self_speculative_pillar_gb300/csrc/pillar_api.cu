@@ -171,6 +171,33 @@ int pillar_topk_select(const pillar_shape_t *shape, int32_t V, const float *veri
     return PILLAR_OK;
 }
 
+int pillar_kv_append(const pillar_shape_t *shape, const uint16_t *k_new, const uint16_t *v_new,
+                     const int32_t *slots, int32_t n, uint16_t *k_pool, uint16_t *v_pool, int32_t *device_flags,
+                     void *stream) {
+    const int st = check_shape(shape);
+    if (st != PILLAR_OK) return st;
+    if (n < 0) return PILLAR_ERR_ARG;
+    if (n == 0) return PILLAR_OK;
+    if (!k_new || !v_new || !slots || !k_pool || !v_pool) return PILLAR_ERR_ARG;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+        !aligned(slots, 4) || (device_flags && !aligned(device_flags, 4)))
+        return PILLAR_ERR_ARG;
+    const int nsm = sm_count();
+    if (nsm <= 0) return PILLAR_ERR_CUDA;
+    KvAppendArgs a;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.slots = slots;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.flags = device_flags;
+    a.num_slots = shape->num_slots;
+    a.n = n;
+    a.Hkv = shape->Hkv;
+    a.D = shape->D;
+    return launch_kv_append(a, nsm, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PILLAR_OK : PILLAR_ERR_CUDA;
+}
+
 int pillar_get_error(void *workspace, void *stream, int32_t *flags) {
     if (!workspace || !flags) return PILLAR_ERR_ARG;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);

@@ -74,3 +74,9 @@ def test_workspace_sizes_and_argument_checks(lib):
     assert lib.pillar_attn_unified(ctypes.byref(s0), *([None] * 12), 0, None) == 0
     assert lib.pillar_topk_select(ctypes.byref(s), 0, *([None] * 8), 0, None) == 0
     assert P.pillar_status_string(-4).startswith("device")
+    # pillar_kv_append: host checks before anything is enqueued
+    assert lib.pillar_kv_append(ctypes.byref(s), None, None, None, 0, None, None, None, None) == 0  # no tokens
+    assert lib.pillar_kv_append(ctypes.byref(s), None, None, None, -1, None, None, None, None) == -1
+    assert lib.pillar_kv_append(ctypes.byref(s), None, None, None, 3, None, None, None, None) == -1
+    odd = ctypes.c_void_p(16 + 8)  # not 16-byte aligned
+    assert lib.pillar_kv_append(ctypes.byref(s), odd, odd, odd, 3, odd, odd, None, None) == -1
