@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "pillar_internal.h"
+#include "pillar_kv.h"
 
 namespace {
 

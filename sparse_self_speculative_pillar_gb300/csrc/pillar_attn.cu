@@ -127,7 +127,8 @@ struct Smem {
     static constexpr int off_meta = off_info + kRowLists * (int)sizeof(ItemInfo);
     static constexpr int off_pend = off_meta + kMaxStages * (int)sizeof(StageMeta);
     static constexpr int off_bar = off_pend + kSBuf * 16;
-    // full[8], empty[8], qempty[2], rfull[4], rempty[4], s_full[4], s_free[4], p_full[4], o_free[2], cexit, drain
+    // full and empty [kMaxStages], qempty[2], rfull and rempty [kRowLists], s_full, s_free and p_full [kSBuf],
+    // o_free[2], cexit, drain, o_done[2], epi_full and epi_empty [2 * kEpiWarps]
     static constexpr int NBAR = 2 * kMaxStages + 2 + 2 * kRowLists + 3 * kSBuf + 2 + 2 + 2 + 4 * kEpiWarps;
     static constexpr int off_misc = off_bar + NBAR * 8;
     static constexpr int off_epi = off_misc + 16;  // per (epilogue warp, slot): EpiRec + 32 float2

@@ -155,14 +155,4 @@ struct TopkArgs {
 };
 cudaError_t launch_topk_select(const TopkArgs &a, cudaStream_t st);
 
-struct KvAppendArgs {
-    const uint16_t *k_new, *v_new;
-    const int *slots;
-    uint16_t *k_pool, *v_pool;
-    int *flags;
-    long long num_slots;
-    int n, Hkv, D;
-};
-cudaError_t launch_kv_append(const KvAppendArgs &a, int nsm, cudaStream_t st);
-
 }  // namespace pillar

@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include "pillar_internal.h"
+#include "pillar_kv.h"
 
 namespace pillar {
 
