@@ -157,3 +157,22 @@ def verify_lse_of(res: AttnResult, req_mode, k, Hq, select=None):
     if not rows:
         return np.zeros((0, Hq, k + 1))
     return np.stack(rows, 0)
+
+
+def kv_append(k_pool, v_pool, k_new, v_new, slots):
+    """The pools after appending new tokens ("SparseSpec-MLSys26", Unified
+    batch scheduler + fused attention kernel: page size 1, one slot per
+    token): copies of k_pool / v_pool [num_slots, Hkv, D] in which row
+    slots[i] holds token i's rows k_new[i] / v_new[i]; a slot outside
+    [0, num_slots) is skipped.  Returns (k, v, any_skipped).  One token at a
+    time, in order."""
+    k = np.array(k_pool, copy=True)
+    v = np.array(v_pool, copy=True)
+    skipped = False
+    for i, s in enumerate(np.asarray(slots).tolist()):
+        if 0 <= s < k.shape[0]:
+            k[s] = k_new[i]
+            v[s] = v_new[i]
+        else:
+            skipped = True
+    return k, v, skipped

@@ -468,3 +468,24 @@ def test_topk_of_a_real_verify_recovers_planted_pillars():
         tot += len(sel)
         base += pil.mean() * len(sel)
     assert hits > 3 * base
+
+
+def test_kv_append_pins():
+    """The append writes exactly the listed slots with the new rows, leaves
+    every other row as it was, skips out-of-range slots, and appending the
+    pool's own rows to their own slots changes nothing."""
+    rng = np.random.default_rng(3)
+    k = rng.integers(-9, 9, (12, 2, 4)).astype(np.int16)
+    v = rng.integers(-9, 9, (12, 2, 4)).astype(np.int16)
+    kn = rng.integers(20, 29, (3, 2, 4)).astype(np.int16)
+    vn = rng.integers(30, 39, (3, 2, 4)).astype(np.int16)
+    k2, v2, skipped = oracle.kv_append(k, v, kn, vn, np.array([5, 12, 0], np.int32))
+    assert skipped
+    for s in range(12):
+        want_k = kn[0] if s == 5 else kn[2] if s == 0 else k[s]
+        want_v = vn[0] if s == 5 else vn[2] if s == 0 else v[s]
+        assert np.array_equal(k2[s], want_k) and np.array_equal(v2[s], want_v)
+    assert np.array_equal(k, k2) is False and k.shape == k2.shape  # the inputs are not modified in place
+    same = np.arange(12, dtype=np.int32)
+    k3, v3, skipped = oracle.kv_append(k, v, k, v, same)
+    assert not skipped and np.array_equal(k3, k) and np.array_equal(v3, v)
