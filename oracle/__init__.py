@@ -176,3 +176,43 @@ def kv_append(k_pool, v_pool, k_new, v_new, slots):
         else:
             skipped = True
     return k, v, skipped
+
+
+def draft_lists_after_topk(next_idx, next_cnt, verify_len, phase, slot_table=None, kv_off=None):
+    """Critical lists of the draft steps that follow a verify step
+    ("SparseSpec-MLSys26", PillarAttn: the Top-K of the verify step's exact
+    scores is the critical set of the next k draft steps; the tokens appended
+    since are attended as well).
+
+    For verify request v and KV head h, at draft phase p (p tokens appended
+    since the verify step, whose length was L_v = verify_len[v]), the list is
+    the Top-K positions next_idx[v, h, :next_cnt[v, h]] (all below L_v),
+    followed by the appended positions L_v, ..., L_v + p - 1, in ascending
+    order.  ``phase`` is one p for all requests or one per request.  With
+    ``slot_table`` and ``kv_off`` (request v's slots start at kv_off[v] and
+    cover its L_v + p positions), each listed position's slot is returned as
+    well.  Returns (lists [V, Hkv, n_max] int32, counts [V, Hkv] int32,
+    slots like lists or None); entries past a count are 0."""
+    next_idx = np.asarray(next_idx)
+    next_cnt = np.asarray(next_cnt)
+    V, Hkv = next_cnt.shape
+    Lv = np.asarray(verify_len, np.int64)
+    ph = np.broadcast_to(np.asarray(phase, np.int64), (V,))
+    built = {}
+    n_max = 1
+    for v in range(V):
+        for h in range(Hkv):
+            crit = [int(x) for x in next_idx[v, h, :int(next_cnt[v, h])]]
+            lst = sorted(crit) + [int(Lv[v]) + i for i in range(int(ph[v]))]
+            built[(v, h)] = lst
+            n_max = max(n_max, len(lst))
+    lists = np.zeros((V, Hkv, n_max), np.int32)
+    counts = np.zeros((V, Hkv), np.int32)
+    slots = np.zeros((V, Hkv, n_max), np.int32) if slot_table is not None else None
+    for (v, h), lst in built.items():
+        counts[v, h] = len(lst)
+        for i, pos in enumerate(lst):
+            lists[v, h, i] = pos
+            if slots is not None:
+                slots[v, h, i] = int(slot_table[int(kv_off[v]) + pos])
+    return lists, counts, slots

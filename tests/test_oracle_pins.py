@@ -489,3 +489,46 @@ def test_kv_append_pins():
     same = np.arange(12, dtype=np.int32)
     k3, v3, skipped = oracle.kv_append(k, v, k, v, same)
     assert not skipped and np.array_equal(k3, k) and np.array_equal(v3, v)
+
+
+def test_draft_lists_after_topk_rebuild_the_generator_lists():
+    """The workload generator builds each draft request's list independently
+    (a critical subset of [0, L-p) plus the p newest positions); feeding the
+    oracle that critical subset as the Top-K of a verify step of length L-p
+    gives back exactly the generator's list, and the slots are the slot
+    table's entries for those positions."""
+    import workloads as W
+    w = W.generate(W.scaled("qwen3_8b", B=20, length_scale=0.05, seed_offset=9))
+    for b in np.nonzero(w.req_mode == 0)[0]:
+        p, L = int(w.phase[b]), int(w.req_len[b])
+        gen = [w.sparse_idx[b, h, :w.sparse_cnt[b, h]] for h in range(w.Hkv)]
+        crit = [g[g < L - p] for g in gen]
+        kmax = max(1, max(len(c) for c in crit))
+        nidx = np.zeros((1, w.Hkv, kmax), np.int32)
+        ncnt = np.zeros((1, w.Hkv), np.int32)
+        for h, c in enumerate(crit):
+            nidx[0, h, :len(c)] = c[::-1]  # any order in: the list comes out ascending
+            ncnt[0, h] = len(c)
+        lists, counts, slots = oracle.draft_lists_after_topk(nidx, ncnt, [L - p], p, slot_table=w.slot_table,
+                                                             kv_off=[w.kv_off[b]])
+        for h in range(w.Hkv):
+            assert np.array_equal(lists[0, h, :counts[0, h]], gen[h])
+            for i in range(counts[0, h]):
+                assert slots[0, h, i] == w.slot_table[w.kv_off[b] + lists[0, h, i]]
+
+
+def test_draft_lists_after_topk_shape_rules():
+    nidx = np.array([[[7, 2, 9], [0, 0, 0]], [[4, 0, 0], [1, 3, 0]]], np.int32)
+    ncnt = np.array([[3, 0], [1, 2]], np.int32)
+    lists, counts, slots = oracle.draft_lists_after_topk(nidx, ncnt, [10, 6], [2, 0])
+    assert slots is None
+    assert counts.tolist() == [[5, 2], [1, 2]]
+    assert lists[0, 0, :5].tolist() == [2, 7, 9, 10, 11]  # Top-K ascending, then the two appended positions
+    assert lists[0, 1, :2].tolist() == [10, 11]            # an empty Top-K keeps the appended positions
+    assert lists[1, 0, :1].tolist() == [4] and lists[1, 1, :2].tolist() == [1, 3]  # phase 0: the Top-K alone
+    ident = np.arange(64, dtype=np.int32)
+    _, _, s2 = oracle.draft_lists_after_topk(nidx, ncnt, [10, 6], 3, slot_table=ident, kv_off=[0, 20])
+    l3, c3, _ = oracle.draft_lists_after_topk(nidx, ncnt, [10, 6], 3)
+    for h in range(2):
+        assert s2[0, h, :c3[0, h]].tolist() == l3[0, h, :c3[0, h]].tolist()  # request 0's slots start at 0
+        assert s2[1, h, :c3[1, h]].tolist() == [20 + x for x in l3[1, h, :c3[1, h]]]  # request 1's at 20
