@@ -2,6 +2,7 @@
 // workspace carving, launches.  Every check that can be made on the host is
 // made here, before anything is enqueued; data-dependent checks are made on
 // the device and reported through the workspace error word.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -32,6 +33,17 @@ int check_shape(const pillar_shape_t *s) {
         if (c != 0 && (c < kTileKeys || c > kMaxChunk || c % kTileKeys != 0)) return PILLAR_ERR_ARG;
     if ((long long)s->B * s->Hkv > (1ll << 30) || (long long)s->max_len * s->Hq * (s->k + 1) > (1ll << 40))
         return PILLAR_ERR_ARG;
+    // The attention workspace must be sizeable in 64 bits with room to spare: its largest
+    // section holds, per work item, (k+1)*G partial rows of D fp32 values (+ LSE), and a
+    // (request, KV head) has at most max(max_len / verify chunk, max_sparse / draft chunk) + 1
+    // items.  Shapes whose bound passes 2^50 bytes are refused rather than wrapped.
+    const long double vc = s->verify_chunk > 0 ? s->verify_chunk : kTileKeys;
+    const long double dc = s->draft_chunk > 0 ? s->draft_chunk : kTileKeys;
+    const long double per_unit = std::max((long double)s->max_len / vc, (long double)s->max_sparse / dc) + 2.0L;
+    const long double rows = (long double)(s->k + 1) * G;
+    const long double bound = (long double)s->B * s->Hkv * per_unit * (rows * (s->D + 1) * 4.0L + 64.0L) +
+                              (long double)s->B * 64.0L + 65536.0L;
+    if (bound > 1125899906842624.0L) return PILLAR_ERR_ARG;  // 2^50
     return PILLAR_OK;
 }
 
@@ -127,6 +139,7 @@ int pillar_topk_workspace_bytes(const pillar_shape_t *shape, int32_t V, size_t *
     const int st = check_shape(shape);
     if (st != PILLAR_OK) return st;
     if (!bytes || V < 0) return PILLAR_ERR_ARG;
+    if ((long double)V * shape->Hkv * shape->max_len * 4.0L > 1125899906842624.0L) return PILLAR_ERR_ARG;  // 2^50
     *bytes = topk_ws_bytes(*shape, V);
     return PILLAR_OK;
 }

@@ -61,6 +61,16 @@ def test_workspace_sizes_and_argument_checks(lib):
         with pytest.raises(P.PillarError) as e:
             P.pillar_attn_workspace_bytes(_shape(**bad))
         assert e.value.status == -1
+    # shapes whose workspace size would not fit in 64 bits are refused, not wrapped
+    huge = _shape(B=1 << 27, Hq=64, Hkv=8, k=7, max_len=(1 << 31) - 1, verify_chunk=64, max_sparse=0)
+    with pytest.raises(P.PillarError) as e:
+        P.pillar_attn_workspace_bytes(huge)
+    assert e.value.status == -1
+    with pytest.raises(P.PillarError) as e:
+        P.pillar_topk_workspace_bytes(_shape(max_len=1 << 30), (1 << 31) - 1)
+    assert e.value.status == -1
+    big = _shape(B=512, k=12, Hq=32, Hkv=8, max_len=32768, max_sparse=4096)  # large but real
+    assert P.pillar_attn_workspace_bytes(big) > 0
     s = _shape()
     # null workspace -> -2, with no device work enqueued
     st = lib.pillar_attn_unified(ctypes.byref(s), *([ctypes.c_void_p(16)] * 11), None, 0, None)
