@@ -113,7 +113,8 @@ typedef struct pillar_shape {
 /*
  * pillar_attn_workspace_bytes -- bytes of workspace pillar_attn_unified
  * needs for this shape (a bound over every batch with req_len <= max_len and
- * sparse_cnt <= max_sparse).  Returns PILLAR_OK or PILLAR_ERR_ARG.
+ * sparse_cnt <= max_sparse).  Returns PILLAR_OK or PILLAR_ERR_ARG (a bad
+ * shape, or one whose workspace bound would pass 2^50 bytes).
  */
 PILLAR_API int pillar_attn_workspace_bytes(const pillar_shape_t *shape, size_t *bytes);
 
@@ -156,7 +157,8 @@ PILLAR_API int pillar_attn_unified(const pillar_shape_t *shape, const uint16_t *
 
 /*
  * pillar_topk_workspace_bytes -- workspace of pillar_topk_select for V
- * verify requests of length <= max_len.
+ * verify requests of length <= max_len.  Returns PILLAR_OK or PILLAR_ERR_ARG
+ * (a bad shape, V < 0, or V * Hkv * max_len fp32 scores past 2^50 bytes).
  */
 PILLAR_API int pillar_topk_workspace_bytes(const pillar_shape_t *shape, int32_t V, size_t *bytes);
 
