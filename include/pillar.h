@@ -145,6 +145,9 @@ PILLAR_API int pillar_attn_workspace_bytes(const pillar_shape_t *shape, size_t *
  *   verify_lse   [V][Hq][k+1] fp32: natural-log LSE of each verify row.
  *   workspace    device scratch of at least pillar_attn_workspace_bytes,
  *                256-byte aligned.  Must not be shared by concurrent calls.
+ * All pointers are device memory.  Alignment: q, k_pool and v_pool 16 bytes,
+ * verify_logits 8 bytes (pairs of logits are stored together), out and the
+ * int32 and fp32 arrays 4 bytes; a misaligned pointer is PILLAR_ERR_ARG.
  *
  * Returns PILLAR_OK, PILLAR_ERR_ARG, PILLAR_ERR_WORKSPACE or PILLAR_ERR_CUDA.
  * With B == 0 nothing is launched.

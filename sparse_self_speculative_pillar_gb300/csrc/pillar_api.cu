@@ -85,8 +85,12 @@ int pillar_attn_unified(const pillar_shape_t *shape, const uint16_t *q, const ui
         !verify_logits || !verify_lse)
         return PILLAR_ERR_ARG;
     if (s.max_sparse > 0 && !sparse_idx) return PILLAR_ERR_ARG;
-    // TMA and 16-byte copies need 16-byte aligned rows
-    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 4)) return PILLAR_ERR_ARG;
+    // TMA and 16-byte copies need 16-byte aligned rows; the logit dump stores pairs (8 bytes);
+    // everything else is read or written in 4-byte words
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 4) ||
+        !aligned(verify_logits, 8) || !aligned(verify_lse, 4) || !aligned(slot_table, 4) || !aligned(req_mode, 4) ||
+        !aligned(req_len, 4) || !aligned(sparse_cnt, 4) || (sparse_idx && !aligned(sparse_idx, 4)))
+        return PILLAR_ERR_ARG;
     const AttnLayout lay = attn_layout(s);
     if (!workspace || !aligned(workspace, 256) || ws_bytes < lay.total) return PILLAR_ERR_WORKSPACE;
     const int nsm = sm_count();

@@ -79,6 +79,11 @@ def test_workspace_sizes_and_argument_checks(lib):
     st = lib.pillar_attn_unified(ctypes.byref(s), None, *([ctypes.c_void_p(16)] * 10), ctypes.c_void_p(256), 1 << 40,
                                  None)
     assert st == -1
+    # a logits pointer that is 4- but not 8-byte aligned -> -1 (pairs of logits are stored together)
+    ptrs = [ctypes.c_void_p(256)] * 11
+    ptrs[9] = ctypes.c_void_p(256 + 4)
+    st = lib.pillar_attn_unified(ctypes.byref(s), *ptrs, ctypes.c_void_p(256), 1 << 40, None)
+    assert st == -1
     # B == 0 -> nothing to do
     s0 = _shape(B=0)
     assert lib.pillar_attn_unified(ctypes.byref(s0), *([None] * 12), 0, None) == 0
