@@ -163,6 +163,9 @@ int pillar_topk_select(const pillar_shape_t *shape, int32_t V, const float *veri
     }
     if (!verify_logits || !verify_lse || !req_len || !group_map || !K || !next_idx || !next_cnt)
         return PILLAR_ERR_ARG;
+    if (!aligned(verify_logits, 4) || !aligned(verify_lse, 4) || !aligned(req_len, 4) || !aligned(group_map, 4) ||
+        !aligned(K, 4) || !aligned(next_idx, 4) || !aligned(next_cnt, 4))
+        return PILLAR_ERR_ARG;  // every array is read or written in 4-byte words
     if (!workspace || !aligned(workspace, 256) || ws_bytes < topk_ws_bytes(*shape, V)) return PILLAR_ERR_WORKSPACE;
     if ((long long)V * shape->Hkv > 65535ll * 65535ll || V > 65535) return PILLAR_ERR_ARG;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);

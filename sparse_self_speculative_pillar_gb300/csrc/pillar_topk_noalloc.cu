@@ -12,6 +12,7 @@
 // inputs and outputs.  Every GPU that loads the library holds the array
 // until the process exits.
 #include <cstdint>
+#include <initializer_list>
 #include <cuda_runtime.h>
 #include <mutex>
 
@@ -60,6 +61,10 @@ int pillar_topk_select_noalloc(const pillar_shape_t *shape, int32_t V, const flo
     if (need > (size_t)PILLAR_NOALLOC_SCRATCH_BYTES) return PILLAR_ERR_SCRATCH;
     if (V > 0 && (!verify_logits || !verify_lse || !req_len || !group_map || !K || !next_idx || !next_cnt))
         return PILLAR_ERR_ARG;
+    for (const void *ptr : {(const void *)verify_logits, (const void *)verify_lse, (const void *)req_len,
+                            (const void *)group_map, (const void *)K, (const void *)next_idx,
+                            (const void *)next_cnt, (const void *)device_flags})
+        if (reinterpret_cast<uintptr_t>(ptr) & 3u) return PILLAR_ERR_ARG;  // 4-byte words throughout
     if ((long long)V * shape->Hkv > 65535ll * 65535ll || V > 65535) return PILLAR_ERR_ARG;
     char *ws = static_cast<char *>(scratch_for_current_device());
     if (!ws) return PILLAR_ERR_CUDA;

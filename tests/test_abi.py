@@ -84,6 +84,11 @@ def test_workspace_sizes_and_argument_checks(lib):
     ptrs[9] = ctypes.c_void_p(256 + 4)
     st = lib.pillar_attn_unified(ctypes.byref(s), *ptrs, ctypes.c_void_p(256), 1 << 40, None)
     assert st == -1
+    # Top-K: a pointer that is not 4-byte aligned -> -1, before anything is enqueued
+    tptr = [ctypes.c_void_p(256)] * 7
+    tptr[5] = ctypes.c_void_p(256 + 2)
+    assert lib.pillar_topk_select(ctypes.byref(s), 3, *tptr, ctypes.c_void_p(256), 1 << 40, None) == -1
+    assert lib.pillar_topk_select_noalloc(ctypes.byref(s), 3, *tptr, None, None) == -1
     # B == 0 -> nothing to do
     s0 = _shape(B=0)
     assert lib.pillar_attn_unified(ctypes.byref(s0), *([None] * 12), 0, None) == 0
