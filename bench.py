@@ -25,6 +25,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -116,8 +117,9 @@ class Clocks:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv") if os.path.isdir(
-            os.path.join(ROOT, "gpurun_out")) else f"/tmp/pillar_clocks_{os.getpid()}.csv"
+        # the samples go to a scratch file; PILLAR_CLOCKS_CSV names a place to keep them instead
+        self.path = os.environ.get("PILLAR_CLOCKS_CSV") or os.path.join(
+            tempfile.gettempdir(), f"pillar_clocks_{os.getpid()}_{index}.csv")
 
     def start(self):
         try:
