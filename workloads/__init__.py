@@ -99,9 +99,6 @@ def _recipes():
 
 
 RECIPES = _recipes()
-# Position of each workload in the published config list (0 = tiny case).
-CONFIG_INDEX = {"tiny": 0, "qwen3_1p7b": 1, "qwen3_8b": 2, "qwen3_14b": 3, "stress": 4,
-                "stress_all_draft": 4, "stress_all_verify": 4}
 
 
 def scaled(name: str, B: int | None = None, length_scale: float = 1.0, seed_offset: int = 0,
