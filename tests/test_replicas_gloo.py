@@ -108,3 +108,23 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     with contextlib.redirect_stdout(out):
         assert bench.run_reference(args) == 0
     assert out.getvalue() == ""  # the other ranks exit without work and print nothing
+
+
+def test_reference_arm_line_on_rank_zero(monkeypatch):
+    """The reference arm (the fp64 oracle on the host cores) prints one JSON
+    line with the keys the bench contract asks of it."""
+    import json
+    import bench
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    args = argparse.Namespace(workload="tiny", gpus=1, steps=2, warmup=1)
+    out = io.StringIO()
+    with contextlib.redirect_stdout(out):
+        assert bench.run_reference(args) == 0
+    line = json.loads(out.getvalue().strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["value"] > 0 and line["higher_is_better"] is False and line["steps"] == 2
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"] == "tiny"
