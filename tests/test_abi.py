@@ -5,6 +5,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 import sparse_self_speculative_pillar_gb300 as P
@@ -100,3 +101,31 @@ def test_workspace_sizes_and_argument_checks(lib):
     assert lib.pillar_kv_append(ctypes.byref(s), None, None, None, 3, None, None, None, None) == -1
     odd = ctypes.c_void_p(16 + 8)  # not 16-byte aligned
     assert lib.pillar_kv_append(ctypes.byref(s), odd, odd, odd, 3, odd, odd, None, None) == -1
+
+
+def test_workspace_covers_the_most_items_the_planner_can_emit():
+    """The planner splits a verify request of L keys into ceil(L / chunk)
+    items (chunk = verify_chunk, or by default 1024 keys below 8192 positions
+    and 2048 from there on) and a draft list of n keys into ceil(n /
+    draft_chunk) items; every item of a split (request, KV head) writes
+    (k+1)*G partial rows of D fp32 values plus an LSE.  The workspace must
+    hold that many item records and partial rows for the worst batch of the
+    shape."""
+    rng = np.random.default_rng(21)
+    for _ in range(200):
+        Hkv = int(rng.integers(1, 9))
+        G = int(rng.integers(1, 9))
+        k = int(rng.integers(0, 64 // G))
+        D = int(rng.choice([64, 128]))
+        vc = int(rng.choice([0, 64, 128, 1024, 2048]))
+        dc = int(rng.choice([0, 64, 512, 2048]))
+        s = _shape(B=int(rng.integers(1, 300)), Hq=G * Hkv, Hkv=Hkv, D=D, k=k,
+                   max_len=int(rng.integers(1, 40000)), max_sparse=int(rng.integers(0, 5000)),
+                   verify_chunk=vc, draft_chunk=dc, row_lo=min(1, k), row_hi=k + 1)
+        units = s.B * Hkv
+        v_items = -(-s.max_len // (vc or 1024))          # the default's smaller chunk gives the most items
+        d_items = -(-s.max_sparse // (dc or 1024)) if s.max_sparse else 1
+        items = units * max(v_items, d_items, 1)
+        rows = items * (k + 1) * G
+        need = items * 16 + rows * (D + 1) * 4              # item records + partial rows (D values + LSE)
+        assert P.pillar_attn_workspace_bytes(s) >= need
