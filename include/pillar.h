@@ -16,9 +16,11 @@
  * + fused attention kernel").
  *
  * Conventions for every entry point:
- *   - All array pointers are DEVICE pointers owned by the caller.  The
- *     library allocates nothing and keeps no state between calls, except the
- *     per-device launch attributes it sets once.  Scratch lives in the
+ *   - All array pointers are DEVICE pointers owned by the caller (the
+ *     phase-bucket functions at the end work on host memory).  The library
+ *     allocates nothing and keeps no state between calls, except the
+ *     per-device launch attributes it sets once and the scratch array of
+ *     pillar_topk_select_noalloc.  Scratch lives in the
  *     caller's workspace (sized by the *_workspace_bytes functions); the
  *     device error word sits inside that workspace.
  *   - bf16 tensors are passed as uint16_t bit patterns.
