@@ -18,9 +18,9 @@
  * Conventions for every entry point:
  *   - All array pointers are DEVICE pointers owned by the caller (the
  *     phase-bucket functions at the end work on host memory).  The library
- *     allocates nothing and keeps no state between calls, except the
- *     per-device launch attributes it sets once and the scratch array of
- *     pillar_topk_select_noalloc.  Scratch lives in the
+ *     allocates nothing and keeps no state between calls, except the launch
+ *     attributes it sets once per device context (up to 64 devices) and the
+ *     scratch array of pillar_topk_select_noalloc.  Scratch lives in the
  *     caller's workspace (sized by the *_workspace_bytes functions); the
  *     device error word sits inside that workspace.
  *   - bf16 tensors are passed as uint16_t bit patterns.
@@ -179,6 +179,10 @@ PILLAR_API int pillar_topk_workspace_bytes(const pillar_shape_t *shape, int32_t 
  *   req_len        [B] int32, as given to pillar_attn_unified.
  *   group_map      [V] int32: batch index b of the v-th verify request, in
  *                  increasing order (it fixes L_v and the logits offsets).
+ *                  A request whose entry lies outside [0, B), or whose
+ *                  length is negative or above max_len, is skipped
+ *                  (next_cnt 0) and flagged PILLAR_FLAG_REQUEST; it counts
+ *                  as length 0 in the offsets of the requests after it.
  *   K              [V] int32: K_v, the number of positions to keep; clamped
  *                  to [0, L_v], and to max_topk with PILLAR_FLAG_TOPK.
  *   next_idx       [V, Hkv, max_topk] int32: the selected positions of KV
@@ -187,8 +191,9 @@ PILLAR_API int pillar_topk_workspace_bytes(const pillar_shape_t *shape, int32_t 
  * For KV head g and position t in [0, L_v):
  *   score[t] = 1/((row_hi-row_lo)*G) * sum_{r in [row_lo,row_hi)}
  *              sum_{h in group g} exp(logit[h][r][t] - lse[h][r])
- * (masked logits contribute 0).  The K_v largest scores are kept, equal
- * scores taken lowest position first.  Scores are formed in fp32.
+ * (masked logits contribute 0, and so does a row that saw no position,
+ * whose LSE is -inf).  The K_v largest scores are kept, equal scores taken
+ * lowest position first.  Scores are formed in fp32.
  */
 PILLAR_API int pillar_topk_select(const pillar_shape_t *shape, int32_t V, const float *verify_logits,
                        const float *verify_lse, const int32_t *req_len, const int32_t *group_map,
@@ -219,9 +224,10 @@ PILLAR_API int pillar_topk_select(const pillar_shape_t *shape, int32_t V, const 
  * > PILLAR_NOALLOC_SCRATCH_BYTES, about V * Hkv * max_len > 4M scores);
  * otherwise as pillar_topk_select.
  *
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Every call shares the one array: calls whose work overlaps on
+ * The first call in a device's context looks up the array's device address
+ * (once per device context, with that device current: a context created
+ * anew, after cudaDeviceReset for instance, gets a lookup of its own); make
+ * that first call before any stream capture.  Every call shares the one array: calls whose work overlaps on
  * the GPU (different streams, or different host threads on one device) race
  * on it and must be serialised by the caller.  Each call clears the error
  * word itself; the score rows are fully rewritten before they are read.

@@ -5,10 +5,42 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cuda.h>  // CUcontext, CUresult (driver entry points are resolved through the runtime)
 #include <cuda_runtime.h>
 
 #include "pillar_internal.h"
 #include "pillar_kv.h"
+
+namespace pillar {
+
+namespace {
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+void *driver_entry(const char *name, int version) {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &f, version, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return f;
+}
+}  // namespace
+
+cudaError_t current_device_context(int *dev, unsigned long long *ctx_id) {
+    static const CtxGetCurrentFn get_current = reinterpret_cast<CtxGetCurrentFn>(driver_entry("cuCtxGetCurrent", 4000));
+    static const CtxGetIdFn get_id = reinterpret_cast<CtxGetIdFn>(driver_entry("cuCtxGetId", 12000));
+    *ctx_id = 0;
+    const cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return e;
+    CUcontext c = nullptr;
+    if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c) return cudaSuccess;
+    unsigned long long id = 0;
+    if (get_id(c, &id) == CUDA_SUCCESS) *ctx_id = id;
+    return cudaSuccess;
+}
+
+}  // namespace pillar
 
 namespace {
 
@@ -179,6 +211,7 @@ int pillar_topk_select(const pillar_shape_t *shape, int32_t V, const float *veri
     ta.next_cnt = next_cnt;
     ta.ws = static_cast<char *>(workspace);
     ta.scores = reinterpret_cast<float *>(ta.ws + topk_scores_offset());
+    ta.B = shape->B;
     ta.V = V;
     ta.Hq = shape->Hq;
     ta.Hkv = shape->Hkv;

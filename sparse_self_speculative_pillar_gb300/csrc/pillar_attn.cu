@@ -335,9 +335,12 @@ __device__ void loader(const AttnParams &p, const Ctx &c, int lane, int li) {
     int stage = 0, qn = 0;
     uint32_t phase = 0, qph = 0, fph = 0, issued = 0, issued_par = 0;
     bool ok = true;
-    // this lane's gather4: row group rgl of the warp's rows, K (kv 0) or V (kv 1), column half h
-    const int rgl = lane % GW, kv = (lane / GW) & 1, h = lane / (2 * GW);
-    const bool gl = h < NH;
+    // this lane's gather4: row group rgl of the warp's rows, K (kv 0) or V (kv 1), column half h.
+    // The column halves of a row group go to adjacent lanes, so the two 128-byte halves of each
+    // 256-byte row are requested back to back and reach DRAM as one access (halves requested
+    // apart behave as random 128-byte reads, which DRAM serves far below its copy rate).
+    const int h = lane % NH, kv = (lane / NH) & 1, rgl = lane / (2 * NH);
+    const bool gl = rgl < GW;
     // K and V rows are read once: evicted first, so that the verify logits written meanwhile
     // are still in L2 when the Top-K pass reads them
     const uint64_t kv_policy = l2_evict_first_policy();
@@ -1089,12 +1092,14 @@ __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(const AttnParam
 
 template <int D>
 cudaError_t launch_unified_t(const AttnParams &p, int nsm, cudaStream_t st) {
-    static int configured_mask = 0;  // one bit per device (up to 32)
+    // launch attributes, once per device context
+    static unsigned long long configured[kMaxDevices] = {};
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    unsigned long long ctx = 0;
+    cudaError_t e = current_device_context(&dev, &ctx);
     if (e != cudaSuccess) return e;
-    const int bit = 1 << (dev & 31);
-    if (!(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & bit)) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (ctx == 0 || __atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE) != ctx) {
         e = cudaFuncSetAttribute(unified_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<D>::total);
         if (e != cudaSuccess) return e;
         int n = 0;
@@ -1102,7 +1107,9 @@ cudaError_t launch_unified_t(const AttnParams &p, int nsm, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         // exactly one CTA per SM: it allocates all of the SM's tensor memory
         if (n != 1) return cudaErrorInvalidConfiguration;
-        __atomic_fetch_or(&configured_mask, bit, __ATOMIC_RELEASE);
+        e = current_device_context(&dev, &ctx);  // (the calls above made a context current)
+        if (e != cudaSuccess) return e;
+        __atomic_store_n(&configured[dev], ctx, __ATOMIC_RELEASE);
     }
     // Both kernels are launched as programmatic dependents of the one before
     // them on the stream: their launch and prologue overlap its tail.

@@ -79,6 +79,15 @@ struct AttnLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// One-time per-context set-up (launch attributes, symbol addresses).  A
+// device's context is told apart by its process-unique id (cuCtxGetId), so
+// a context re-created after cudaDeviceReset is set up again.
+constexpr int kMaxDevices = 64;
+
+// The current device and the unique id of the context current on it (0
+// when no context is current yet: the caller then sets up and asks again).
+cudaError_t current_device_context(int *dev, unsigned long long *ctx_id);
+
 // 0: the default, chosen per request by its context length (see kLongContext)
 inline int verify_chunk_of(const pillar_shape_t &s) { return s.verify_chunk > 0 ? s.verify_chunk : 0; }
 inline int draft_chunk_of(const pillar_shape_t &s) { return s.draft_chunk > 0 ? s.draft_chunk : kDefaultDraftChunk; }
@@ -151,7 +160,7 @@ struct TopkArgs {
     int *next_idx, *next_cnt;
     char *ws;
     float *scores;
-    int V, Hq, Hkv, k, row_lo, row_hi, max_topk, max_len;
+    int B, V, Hq, Hkv, k, row_lo, row_hi, max_topk, max_len;
 };
 cudaError_t launch_topk_select(const TopkArgs &a, cudaStream_t st);
 

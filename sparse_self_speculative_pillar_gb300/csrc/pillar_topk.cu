@@ -30,8 +30,15 @@ struct TopkParams {
     int *next_idx, *next_cnt;
     WsHeader *hdr;
     float *scores;
-    int V, Hq, Hkv, G, k, row_lo, row_hi, max_topk, max_len, smem_keys;
+    int B, V, Hq, Hkv, G, k, row_lo, row_hi, max_topk, max_len, smem_keys;
 };
+
+// L_v of verify request v, or -1 when group_map[v] names no request of the
+// batch (that request is then skipped and flagged).
+__device__ __forceinline__ int verify_len(const TopkParams &p, int v) {
+    const int b = p.group_map[v];
+    return (b >= 0 && b < p.B) ? p.req_len[b] : -1;
+}
 
 constexpr int kScoreThreads = 256;
 constexpr int kScorePerThread = 2;
@@ -42,16 +49,18 @@ constexpr int kSelectSmemKeys = 40 * 1024;  // keys kept in shared memory (160 K
 constexpr int kSelectWarps = kSelectThreads / 32;
 
 // Offsets of verify request v in the packed logits (sums over v' < v of
-// Hq*(k+1)*L_v') and in the scores scratch (sums of Hkv*min(L_v', max_len),
-// so that a bad length can never push a later request past the workspace).
+// Hq*(k+1)*max(L_v', 0), the offsets the attention planner gives the dump)
+// and in the scores scratch (sums of Hkv*min(max(L_v', 0), max_len), so that
+// a bad length can never push a later request past the workspace).  A request
+// whose group_map entry is out of range counts as length 0.
 // Warp 0 computes them; every thread of the block gets them.
 __device__ void verify_offsets(const TopkParams &p, int v, long long *lg_off, long long *sc_off) {
     __shared__ long long s_off[2];
     if (threadIdx.x < 32) {
         long long s = 0, c = 0;
         for (int i = threadIdx.x; i < v; i += 32) {
-            const int l = p.req_len[p.group_map[i]];
-            s += l;
+            const int l = verify_len(p, i);
+            s += l < 0 ? 0 : l;
             c += l < 0 ? 0 : (l > p.max_len ? p.max_len : l);
         }
 #pragma unroll
@@ -107,7 +116,7 @@ __global__ void __launch_bounds__(kScoreThreads) topk_scores_kernel(const TopkPa
     pdl_launch_dependents();
     pdl_wait_prerequisites();
     const int v = blockIdx.z, g = blockIdx.y;
-    const int L = p.req_len[p.group_map[v]];
+    const int L = verify_len(p, v);
     const int t0 = blockIdx.x * kScoreChunk;
     if (L < 0 || L > p.max_len) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&p.hdr->err, PILLAR_FLAG_REQUEST);
@@ -119,14 +128,16 @@ __global__ void __launch_bounds__(kScoreThreads) topk_scores_kernel(const TopkPa
     const int R = p.row_hi - p.row_lo, nrows = R * p.G;
     const int nrows_pad = (nrows + kScoreRowBatch - 1) / kScoreRowBatch * kScoreRowBatch;
     // per averaged row: its offset in the logits and 24 - lse*log2(e); the
-    // padding rows repeat row 0's offset and contribute 2^-inf = 0
+    // padding rows repeat row 0's offset and contribute 2^-inf = 0, and so
+    // does a row that saw no position (LSE -inf, every logit -inf)
     __shared__ float s_c[kMaxRows];
     __shared__ long long s_row[kMaxRows];
     static_assert(kMaxRows % kScoreRowBatch == 0 && kMaxRows <= kScoreThreads, "row tables");
     if (threadIdx.x < nrows_pad) {
         const int i = threadIdx.x, ir = i < nrows ? i : 0;
         const int h = g * p.G + ir / R, r = p.row_lo + ir % R;
-        s_c[i] = i < nrows ? kExpOffset - p.lse[((long long)v * p.Hq + h) * (p.k + 1) + r] * kLog2e : neg_inf();
+        const float lse = i < nrows ? p.lse[((long long)v * p.Hq + h) * (p.k + 1) + r] : neg_inf();
+        s_c[i] = lse > neg_inf() ? kExpOffset - lse * kLog2e : neg_inf();
         s_row[i] = lg_off + ((long long)h * (p.k + 1) + r) * L;
     }
     __syncthreads();
@@ -186,7 +197,7 @@ __global__ void __launch_bounds__(kSelectThreads, 1) topk_select_kernel(const To
     const int v = blockIdx.y, g = blockIdx.x, tid = threadIdx.x;
     __shared__ int s_lk[2];
     if (tid == 32) {  // the request's length and budget, read while warp 0 sums the offsets
-        s_lk[0] = p.req_len[p.group_map[v]];
+        s_lk[0] = verify_len(p, v);
         s_lk[1] = p.K[v];
     }
     long long lg_off, sc_off;
@@ -329,6 +340,7 @@ cudaError_t launch_topk_select(const TopkArgs &a, cudaStream_t st) {
     p.next_cnt = a.next_cnt;
     p.hdr = reinterpret_cast<WsHeader *>(a.ws);
     p.scores = a.scores;
+    p.B = a.B;
     p.V = a.V;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
@@ -340,17 +352,21 @@ cudaError_t launch_topk_select(const TopkArgs &a, cudaStream_t st) {
     p.max_len = a.max_len;
     p.smem_keys = min(a.max_len, kSelectSmemKeys);
     if (p.V == 0) return cudaSuccess;
-    static int configured_mask = 0;
+    // launch attributes, once per device context
+    static unsigned long long configured[kMaxDevices] = {};
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    unsigned long long ctx = 0;
+    cudaError_t e = current_device_context(&dev, &ctx);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     const size_t sel_smem = sizeof(uint32_t) * (size_t)p.smem_keys;
-    const int bit = 1 << (dev & 31);
-    if (!(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & bit)) {
+    if (ctx == 0 || __atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE) != ctx) {
         e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)(sizeof(uint32_t) * kSelectSmemKeys));
         if (e != cudaSuccess) return e;
-        __atomic_fetch_or(&configured_mask, bit, __ATOMIC_RELEASE);
+        e = current_device_context(&dev, &ctx);
+        if (e != cudaSuccess) return e;
+        __atomic_store_n(&configured[dev], ctx, __ATOMIC_RELEASE);
     }
     // Both kernels are programmatic dependents of the one before them on the
     // stream: their launch overlaps its tail, and each waits for it to

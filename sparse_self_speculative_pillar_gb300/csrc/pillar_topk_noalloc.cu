@@ -28,22 +28,31 @@ using namespace pillar;
 // for the device copy; the device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_topk_scratch[PILLAR_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddr {
+    unsigned long long ctx;  // unique id of the context the address belongs to (0: none yet)
+    void *ptr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
 
-// Once per device, with that device current: the device address of the
-// scratch array.  Returns nullptr if the runtime cannot provide it.
+// The device address of the scratch array in the context current on the
+// current device, looked up once per device context (so a context created
+// anew after cudaDeviceReset gets its own lookup).  Returns nullptr if the
+// runtime cannot provide it.
 void *scratch_for_current_device() {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    unsigned long long ctx = 0;
+    if (current_device_context(&dev, &ctx) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
+    ScratchAddr &a = g_scratch_addr[dev];
+    if (ctx == 0 || a.ctx != ctx || !a.ptr) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess) return nullptr;
-        g_scratch_ptr[dev] = p;
+        if (current_device_context(&dev, &ctx) != cudaSuccess) return nullptr;  // the lookup made a context current
+        a.ctx = ctx;
+        a.ptr = p;
     }
-    return g_scratch_ptr[dev];
+    return a.ptr;
 }
 
 }  // namespace
@@ -82,6 +91,7 @@ int pillar_topk_select_noalloc(const pillar_shape_t *shape, int32_t V, const flo
         ta.next_cnt = next_cnt;
         ta.ws = ws;
         ta.scores = reinterpret_cast<float *>(ws + topk_scores_offset());
+        ta.B = shape->B;
         ta.V = V;
         ta.Hq = shape->Hq;
         ta.Hkv = shape->Hkv;
