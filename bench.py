@@ -321,7 +321,7 @@ def fusion_ablation(g, P, stream, n):
 def run_gpu(args):
     import torch
     import sparse_self_speculative_pillar_gb300 as P
-    from tests._gpu_common import Gpu
+    from workloads.device import Gpu
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)

@@ -30,7 +30,9 @@
  *     (an index or slot out of range, a bad mode or length) are skipped and
  *     recorded in the error word; read it with pillar_get_error.
  *   - Nothing on the device waits without a bound: a wait that runs past
- *     about one second records PILLAR_FLAG_TIMEOUT and the kernel returns.
+ *     its bound (one second, or the shape's wait_timeout_us) records
+ *     PILLAR_FLAG_TIMEOUT and the kernel returns.  The device error word
+ *     of the workspace is cleared by every call and reports that call only.
  */
 #ifndef PILLAR_H
 #define PILLAR_H
@@ -85,6 +87,13 @@ typedef struct pillar_shape {
     int64_t num_slots;     /* rows of k_pool / v_pool */
     float sm_scale;        /* logit scale; 0 means 1/sqrt(D) */
     int32_t schedule;      /* PILLAR_SCHEDULE_* (0: the unified pass) */
+    int32_t wait_timeout_us; /* bound on every pipeline wait of pillar_attn_unified, in
+                              microseconds (>= 0; 0 means 1000000, one second); a wait that
+                              runs past it records PILLAR_FLAG_TIMEOUT and the kernel
+                              returns with incomplete outputs.  The waits that let copies
+                              and tensor-core work already in flight finish before a CTA
+                              exits keep their own one-second bound. */
+    int32_t reserved;      /* set to 0 */
 } pillar_shape_t;
 
 /*

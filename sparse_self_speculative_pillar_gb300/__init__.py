@@ -55,15 +55,16 @@ class PillarShape(ctypes.Structure):
         ("row_lo", ctypes.c_int32), ("row_hi", ctypes.c_int32), ("max_topk", ctypes.c_int32),
         ("verify_chunk", ctypes.c_int32), ("draft_chunk", ctypes.c_int32), ("num_slots", ctypes.c_int64),
         ("sm_scale", ctypes.c_float), ("schedule", ctypes.c_int32),
+        ("wait_timeout_us", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
 
 def make_shape(*, B, Hq, Hkv, D, k, max_sparse, max_len, num_slots, max_topk=1, row_lo=1, row_hi=None,
-               verify_chunk=0, draft_chunk=0, sm_scale=0.0, schedule=0) -> PillarShape:
+               verify_chunk=0, draft_chunk=0, sm_scale=0.0, schedule=0, wait_timeout_us=0) -> PillarShape:
     return PillarShape(B=B, Hq=Hq, Hkv=Hkv, D=D, k=k, max_sparse=max_sparse, max_len=max_len,
                        row_lo=row_lo, row_hi=(k + 1) if row_hi is None else row_hi, max_topk=max(1, max_topk),
                        verify_chunk=verify_chunk, draft_chunk=draft_chunk, num_slots=num_slots,
-                       sm_scale=sm_scale, schedule=schedule)
+                       sm_scale=sm_scale, schedule=schedule, wait_timeout_us=wait_timeout_us)
 
 
 class PillarBuckets(ctypes.Structure):

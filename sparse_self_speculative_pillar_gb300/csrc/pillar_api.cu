@@ -60,6 +60,7 @@ int check_shape(const pillar_shape_t *s) {
     if (s->Hkv > 0 && s->num_slots > 0x7fffffffll / s->Hkv) return PILLAR_ERR_ARG;
     if (s->row_lo < 0 || s->row_hi > s->k + 1 || s->row_lo >= s->row_hi) return PILLAR_ERR_ARG;
     if (s->schedule < PILLAR_SCHEDULE_UNIFIED || s->schedule > PILLAR_SCHEDULE_UNIFORM_ROWS) return PILLAR_ERR_ARG;
+    if (s->wait_timeout_us < 0) return PILLAR_ERR_ARG;
     if (!(s->sm_scale >= 0.f) || std::isinf(s->sm_scale)) return PILLAR_ERR_ARG;
     for (int c : {s->verify_chunk, s->draft_chunk})
         if (c != 0 && (c < kTileKeys || c > kMaxChunk || c % kTileKeys != 0)) return PILLAR_ERR_ARG;
@@ -167,6 +168,7 @@ int pillar_attn_unified(const pillar_shape_t *shape, const uint16_t *q, const ui
     aa.max_sparse = s.max_sparse;
     aa.schedule = s.schedule;
     aa.scale = s.sm_scale > 0.f ? s.sm_scale : 1.0f / std::sqrt((float)s.D);
+    aa.wait_ns = s.wait_timeout_us > 0 ? (unsigned long long)s.wait_timeout_us * 1000ull : kWaitTimeoutNs;
     if (launch_attn(aa, nsm, cs) != cudaSuccess) return PILLAR_ERR_CUDA;
     return PILLAR_OK;
 }

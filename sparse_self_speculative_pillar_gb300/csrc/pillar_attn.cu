@@ -53,7 +53,7 @@
 //     critical lists) writes normalised partials (o, lse) per item, combined
 //     afterwards by merge_kernel, a flat bandwidth pass:
 //     o = sum_i e^{lse_i - lse} o_i, lse = log sum_i e^{lse_i};
-//   * every wait is bounded (about 1 s); a timeout raises PILLAR_FLAG_TIMEOUT,
+//   * every wait is bounded (1 s unless the shape sets a bound); a timeout raises PILLAR_FLAG_TIMEOUT,
 //     the loaders wait for their copies still in flight, the MMA thread for
 //     its MMAs, the tensor memory is freed and the CTA returns.
 #include <cuda.h>  // CUtensorMap (the encoder is resolved at run time through the runtime)
@@ -80,6 +80,7 @@ struct AttnParams {
     int Hq, Hkv, G, k, M, max_sparse;
     int RQ, RQd;  // query rows per TMEM lane quadrant: verify ceil(M / 4), draft ceil(G / 4)
     float scale;
+    unsigned long long wait_ns;  // bound of every pipeline wait (the drains keep kWaitTimeoutNs)
 };
 
 enum : int { kFirst = 1, kLast = 2, kStop = 4 };
@@ -169,6 +170,7 @@ struct Ctx {
     volatile int *abort;
     uint32_t *tmem_slot;
     int *err;
+    unsigned long long wait_ns;  // bound of every pipeline wait
 };
 
 template <int D>
@@ -200,11 +202,13 @@ __device__ __forceinline__ Ctx make_ctx(char *smem, const AttnParams &p) {
     c.abort = reinterpret_cast<volatile int *>(smem + S::off_misc);
     c.tmem_slot = reinterpret_cast<uint32_t *>(smem + S::off_misc + 4);
     c.err = &p.hdr->err;
+    c.wait_ns = p.wait_ns;
     return c;
 }
 
 // Bounded wait that ignores the abort flag: used only to let copies or MMAs
-// already in flight finish before the CTA exits.
+// already in flight finish before the CTA exits (always the one-second
+// bound, whatever the pipeline waits' bound).
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
     const unsigned long long t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity))
@@ -227,7 +231,7 @@ __device__ void resolver(const AttnParams &p, const Ctx &c, int lane) {
     const int num_items = *reinterpret_cast<volatile int *>(&p.hdr->num_items);
     uint32_t eph = 0;
     for (int rb = 0;; rb = rb + 1 == kRowLists ? 0 : rb + 1) {
-        if (!mbar_wait(&c.rempty[rb], ((eph >> rb) & 1) ^ 1, c.abort, c.err)) return;
+        if (!mbar_wait(&c.rempty[rb], ((eph >> rb) & 1) ^ 1, c.abort, c.err, c.wait_ns)) return;
         eph ^= 1u << rb;
         int it = 0;
         if (lane == 0) it = atomicAdd(&p.hdr->item_counter, 1);
@@ -345,12 +349,12 @@ __device__ void loader(const AttnParams &p, const Ctx &c, int lane, int li) {
     // are still in L2 when the Top-K pass reads them
     const uint64_t kv_policy = l2_evict_first_policy();
     for (int rb = 0;; rb = rb + 1 == kRowLists ? 0 : rb + 1) {
-        ok = mbar_wait(&c.rfull[rb], (fph >> rb) & 1, c.abort, c.err);
+        ok = mbar_wait(&c.rfull[rb], (fph >> rb) & 1, c.abort, c.err, c.wait_ns);
         if (!ok) break;
         fph ^= 1u << rb;
         const ItemInfo info = c.iinfo[rb];
         if (info.it < 0) {
-            ok = mbar_wait(&c.empty[stage], phase ^ 1, c.abort, c.err);
+            ok = mbar_wait(&c.empty[stage], phase ^ 1, c.abort, c.err, c.wait_ns);
             if (ok) {
                 cp_async_arrive_noinc(&c.full[stage]);
                 __syncwarp();
@@ -368,10 +372,10 @@ __device__ void loader(const AttnParams &p, const Ctx &c, int lane, int li) {
         const int qb = qn & 1;  // two query buffers: this item's may still hold the one before last
         ++qn;
         for (int t = 0; t < ntiles; ++t) {
-            ok = mbar_wait(&c.empty[stage], phase ^ 1, c.abort, c.err);
+            ok = mbar_wait(&c.empty[stage], phase ^ 1, c.abort, c.err, c.wait_ns);
             if (!ok) break;
             if (t == 0) {  // every loader writes query rows: the buffer's previous item must be done with it
-                ok = mbar_wait(&c.qempty[qb], ((qph >> qb) & 1) ^ 1, c.abort, c.err);
+                ok = mbar_wait(&c.qempty[qb], ((qph >> qb) & 1) ^ 1, c.abort, c.err, c.wait_ns);
                 if (!ok) break;
                 qph ^= 1u << qb;
             }
@@ -551,7 +555,7 @@ __device__ void mma_issuer(const AttnParams &p, const Ctx &c, uint32_t tbase) {
             const unsigned long long now = global_timer_ns();
             if (t_idle == 0) {
                 t_idle = now;
-            } else if (now - t_idle > kWaitTimeoutNs) {
+            } else if (now - t_idle > c.wait_ns) {
                 atomicOr(c.err, PILLAR_FLAG_TIMEOUT);
                 *c.abort = 1;
                 break;
@@ -580,7 +584,7 @@ struct CState {
 __device__ __forceinline__ bool post_epilogue(const Ctx &c, int warp, int lane, CState &cs, const EpiRec &e, float2 inv) {
     const int slot = warp * 2 + (int)(cs.items & 1);
     const uint32_t use = cs.items >> 1;  // earlier uses of this slot
-    if (!mbar_wait(&c.epi_empty[slot], (use & 1) ^ 1, c.abort, c.err)) return false;
+    if (!mbar_wait(&c.epi_empty[slot], (use & 1) ^ 1, c.abort, c.err, c.wait_ns)) return false;
     if (lane == 0) c.epi[slot] = e;
     c.epi_inv[slot * 32 + lane] = inv;
     __syncwarp();
@@ -744,7 +748,7 @@ __device__ bool attn_item(const AttnParams &p, const Ctx &c, int warp, int lane,
         const uint32_t vt = cs.vt, sb = vt % kSBuf;
         __syncwarp();
         if (lane == 0) mbar_arrive(&c.empty[cs.stage]);  // the stage is read by the tensor cores only
-        if (!mbar_wait(&c.s_full[sb], (vt / kSBuf) & 1, c.abort, c.err)) return false;
+        if (!mbar_wait(&c.s_full[sb], (vt / kSBuf) & 1, c.abort, c.err, c.wait_ns)) return false;
         tc_fence_after();
         const uint32_t tS = cs.tbase + sb * kTileKeys;
         float s[32];
@@ -786,7 +790,7 @@ __device__ bool attn_item(const AttnParams &p, const Ctx &c, int warp, int lane,
         if (__any_sync(0xffffffffu, grow_a || grow_b)) {
             // O holds this item's earlier tiles (a grow needs one): the last P V must have completed
             const uint32_t pv = vt - 1;
-            if (!mbar_wait(&c.s_free[pv % kSBuf], (pv / kSBuf) & 1, c.abort, c.err)) return false;
+            if (!mbar_wait(&c.s_free[pv % kSBuf], (pv / kSBuf) & 1, c.abort, c.err, c.wait_ns)) return false;
             tc_fence_after();
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 64) {
@@ -814,7 +818,7 @@ __device__ bool attn_item(const AttnParams &p, const Ctx &c, int warp, int lane,
             cs.phase ^= 1;
         }
         if (last) break;
-        if (!mbar_wait(&c.full[cs.stage], cs.phase, c.abort, c.err)) return false;
+        if (!mbar_wait(&c.full[cs.stage], cs.phase, c.abort, c.err, c.wait_ns)) return false;
         cur = c.meta[cs.stage];
     }
 
@@ -864,13 +868,13 @@ __device__ void epilogue_warp(const AttnParams &p, const Ctx &c, int q, int lane
     uint32_t odone = 0;  // bit b: parity of O buffer b's next completion
     for (uint32_t n = 0;; ++n) {
         const int slot = q * 2 + (int)(n & 1);
-        if (!mbar_wait(&c.epi_full[slot], (n >> 1) & 1, c.abort, c.err)) break;
+        if (!mbar_wait(&c.epi_full[slot], (n >> 1) & 1, c.abort, c.err, c.wait_ns)) break;
         const EpiRec e = c.epi[slot];
         const float2 inv = c.epi_inv[slot * 32 + lane];
         __syncwarp();
         if (lane == 0) mbar_arrive(&c.epi_empty[slot]);  // the record is copied: the slot may be reused
         if (e.stop) break;
-        if (!mbar_wait(&c.o_done[e.qb], (odone >> e.qb) & 1, c.abort, c.err)) break;
+        if (!mbar_wait(&c.o_done[e.qb], (odone >> e.qb) & 1, c.abort, c.err, c.wait_ns)) break;
         odone ^= 1u << e.qb;
         tc_fence_after();
         ItemInfo in;
@@ -911,7 +915,7 @@ __device__ void consumer(const AttnParams &p, const Ctx &c, int warp, int lane, 
     cs.tbase = tbase;
     cs.items = 0;
     for (;;) {
-        if (!mbar_wait(&c.full[cs.stage], cs.phase, c.abort, c.err)) break;
+        if (!mbar_wait(&c.full[cs.stage], cs.phase, c.abort, c.err, c.wait_ns)) break;
         const StageMeta m = c.meta[cs.stage];
         if (m.flags & kStop) break;
         if (!attn_item<D>(p, c, warp, lane, cs, m)) break;
@@ -1199,6 +1203,7 @@ cudaError_t launch_attn(const AttnArgs &a, int nsm, cudaStream_t st) {
     p.RQd = a.schedule == PILLAR_SCHEDULE_UNIFORM_ROWS ? p.RQ : (p.G + kConsumerWarps - 1) / kConsumerWarps;
     p.max_sparse = a.max_sparse;
     p.scale = a.scale;
+    p.wait_ns = a.wait_ns;
     return a.D == 128 ? launch_unified_t<128>(p, nsm, st) : launch_unified_t<64>(p, nsm, st);
 }
 

@@ -82,16 +82,20 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Bounded: gives
-// up after kWaitTimeoutNs (or as soon as *abort is set by another warp),
-// records PILLAR_FLAG_TIMEOUT in *err and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *err) {
+// up after limit_ns (or as soon as *abort is set by another warp), records
+// PILLAR_FLAG_TIMEOUT in *err and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *err,
+                                          unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
+    // the clock and the abort flag are read every 64 polls under the default bound, every poll under a
+    // short one (a poll may suspend the thread for a while)
+    const uint32_t cadence = limit_ns < 1000000ull ? 0u : 63u;
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63) == 0) {
+        if ((i & cadence) == 0) {
             if (*abort) return false;
-            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 atomicOr(err, PILLAR_FLAG_TIMEOUT);
                 *abort = 1;
                 return false;

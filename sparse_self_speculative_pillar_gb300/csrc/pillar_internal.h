@@ -27,7 +27,7 @@ constexpr int kLongContext = 8192;
 constexpr int kDefaultDraftChunk = 1024;
 constexpr int kMaxChunk = 2048;        // item key bound (sizes the resolved row lists in shared memory)
 constexpr int kPlanThreads = 1024;
-constexpr unsigned long long kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
+constexpr unsigned long long kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s: the default wait bound, and the drains'
 
 // Request and unit records written by the planner.
 struct ReqInfo {
@@ -151,6 +151,7 @@ struct AttnArgs {
     int Hq, Hkv, D, k, max_sparse;
     int schedule;  // PILLAR_SCHEDULE_*
     float scale;
+    unsigned long long wait_ns;  // bound of every pipeline wait
 };
 cudaError_t launch_attn(const AttnArgs &a, int grid, cudaStream_t st);
 

@@ -34,10 +34,11 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_shape_struct_matches_header_layout():
-    # 12 int32, then int64 (8-aligned at 48), float, int32 -> 64 bytes
-    assert ctypes.sizeof(P.PillarShape) == 64
+    # 12 int32, then int64 (8-aligned at 48), float, 3 int32 -> 72 bytes
+    assert ctypes.sizeof(P.PillarShape) == 72
     assert P.PillarShape.num_slots.offset == 48
     assert P.PillarShape.schedule.offset == 60
+    assert P.PillarShape.wait_timeout_us.offset == 64
     # pillar_buckets_t: int32 nbuckets, then PILLAR_MAX_BUCKETS int32 counts
     src = open(os.path.join(ROOT, "include", "pillar.h")).read()
     assert int(re.search(r"#define PILLAR_MAX_BUCKETS (\d+)", src).group(1)) == P.MAX_BUCKETS
@@ -57,7 +58,7 @@ def test_workspace_sizes_and_argument_checks(lib):
         assert P.pillar_attn_workspace_bytes(_shape(schedule=sched)) == n  # the schedule needs no other room
     assert P.pillar_topk_workspace_bytes(_shape(), 3) >= 3 * 8 * 8192 * 4
     for bad in (dict(D=96), dict(Hq=30), dict(k=15, Hq=40, Hkv=8), dict(max_len=0), dict(row_lo=3, row_hi=2),
-                dict(verify_chunk=100), dict(draft_chunk=8192), dict(Hq=72, Hkv=8), dict(schedule=4),
+                dict(verify_chunk=100), dict(draft_chunk=8192), dict(Hq=72, Hkv=8), dict(schedule=4), dict(wait_timeout_us=-1),
                 dict(schedule=-1)):
         with pytest.raises(P.PillarError) as e:
             P.pillar_attn_workspace_bytes(_shape(**bad))
