@@ -11,6 +11,8 @@ synthetic data of that shape (see workloads/).
 Prints one JSON line (rank 0).  value = microseconds per layer-step (lower
 is better); under torchrun every rank runs its own replica of the workload
 (weak scaling) and value = max-over-ranks time / layer-steps of all ranks.
+Consecutive steps rotate over --layers (default 4) copies of the KV pools and
+logit/LSE buffers, as consecutive layers of a model would.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle as the reference arm
@@ -55,6 +57,8 @@ def parse():
     ap.add_argument("--batch", type=int, default=None, help="fewer requests (profiling runs)")
     ap.add_argument("--quick", action="store_true",
                     help="headline loop only: no CPU baseline, no breakdown, no end-to-end pass")
+    ap.add_argument("--layers", type=int, default=4,
+                    help="KV pools (with their logit and LSE buffers) rotated over the timed steps")
     return ap.parse_args()
 
 
@@ -318,6 +322,36 @@ def fusion_ablation(g, P, stream, n):
     return res
 
 
+def kv_append_timing(g, w, P, stream, n):
+    """pillar_kv_append for the new tokens of one step of the workload's mix (k+1
+    per verify request, 1 per draft request), timed over n calls.  The rows
+    written are the pool's own rows at those slots, so the pool is unchanged."""
+    import torch
+    from workloads.device import to_device
+    kvo = w.kv_off
+    idx = []
+    for b in range(w.B):
+        n_new = w.k + 1 if w.req_mode[b] == 1 else 1
+        L = int(w.req_len[b])
+        idx.extend(int(kvo[b]) + t for t in range(L - n_new, L))
+    idx = np.asarray(idx, np.int64)
+    k_new, v_new = to_device(w.k_logical[idx]), to_device(w.v_logical[idx])
+    slots = to_device(w.slot_table[idx].astype(np.int32))
+    dflag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        P.pillar_kv_append(g.shape, k_new, v_new, slots, g.k_pool, g.v_pool, dflag, stream=stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        P.pillar_kv_append(g.shape, k_new, v_new, slots, g.k_pool, g.v_pool, dflag, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / n
+    moved = 2 * len(idx) * w.Hkv * w.D * 2 * 2  # K and V rows read and written
+    return {"tokens": int(len(idx)), "us": us, "gbs": moved / (us * 1e-6) / 1e9, "bytes_moved": moved,
+            "calls": n, "flags": int(dflag.item())}
+
+
 def run_gpu(args):
     import torch
     import sparse_self_speculative_pillar_gb300 as P
@@ -334,13 +368,25 @@ def run_gpu(args):
     g = Gpu(w)
     ab = W.algorithmic_bytes(w)
     stream = torch.cuda.current_stream()
+    # Layer rotation: consecutive steps read the KV pools of different layers (copies of the same
+    # rows at other addresses) and write other logit/LSE buffers, as a model's layers do, so that
+    # no step finds the previous step's pool or dump in L2.
+    n_layers = max(1, args.layers)
+    layers = [(g.k_pool, g.v_pool, g.logits, g.lse)]
+    for _ in range(n_layers - 1):
+        layers.append((g.k_pool.clone(), g.v_pool.clone(), torch.empty_like(g.logits), torch.empty_like(g.lse)))
+    layer_bytes = sum(t.numel() * t.element_size() for t in layers[0])
 
-    def step():
+    def use_layer(i):
+        g.k_pool, g.v_pool, g.logits, g.lse = layers[i % n_layers]
+
+    def step(i):
+        use_layer(i)
         g.attn(stream)
         g.topk(stream)
 
-    for _ in range(max(3, args.warmup)):
-        step()
+    for i in range(max(3, args.warmup)):
+        step(i)
     torch.cuda.synchronize()
     flags = g.attn_flags() | g.topk_flags()
     if flags:
@@ -355,8 +401,8 @@ def run_gpu(args):
     clocks.start()
     time.sleep(0.2)
     start.record(stream)
-    for _ in range(args.steps):
-        step()
+    for i in range(args.steps):
+        step(i)
     stop.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -379,6 +425,7 @@ def run_gpu(args):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nb)]
     torch.cuda.synchronize()
     for i in range(nb):
+        use_layer(i)
         ev[i][0].record(stream)
         g.attn(stream)
         ev[i][1].record(stream)
@@ -414,7 +461,8 @@ def run_gpu(args):
                 d_in[b][n].copy_(h_in[n], non_blocking=True)
         ev_in[b].record(copy)
 
-    def compute(b):
+    def compute(b, s_i=0):
+        use_layer(s_i)
         i, o = d_in[b], d_out[b]
         P.pillar_attn_unified(g.shape, i["q"], g.k_pool, g.v_pool, i["slot_table"], i["req_mode"], i["req_len"],
                               i["sparse_idx"], i["sparse_cnt"], o["out"], g.logits, g.lse, g.ws, stream=stream)
@@ -437,7 +485,7 @@ def run_gpu(args):
     for s_i in range(e2e_steps):
         b = s_i & 1
         stream.wait_event(ev_in[b])  # this step's inputs have landed (and its output set was read back)
-        compute(b)
+        compute(b, s_i)
         if s_i + 1 < e2e_steps:
             if s_i >= 1:
                 copy.wait_event(ev_out[1 - b])  # the step before has finished reading the other input set
@@ -449,15 +497,16 @@ def run_gpu(args):
     # (no overlap), reported beside the pipelined number
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2.record(stream)
-    for _ in range(e2e_steps):
+    for s_i in range(e2e_steps):
         for n in IN:
             d_in[0][n].copy_(h_in[n], non_blocking=True)
-        compute(0)
+        compute(0, s_i)
         for n in OUT:
             h_out[0][n].copy_(d_out[0][n], non_blocking=True)
     e3.record(stream)
     torch.cuda.synchronize()
     serial_us = whole_job_us(max_over_ranks(e2.elapsed_time(e3), world, "cuda"), e2e_steps, world)
+    use_layer(0)
     last = h_out[(e2e_steps - 1) & 1]
     if not (torch.equal(last["next_cnt"], g.next_cnt.cpu()) and torch.equal(last["out"], g.out.cpu())):
         raise RuntimeError("end-to-end results differ from the device-resident run")
@@ -465,6 +514,7 @@ def run_gpu(args):
     e2e_us = whole_job_us(e2e_ms, e2e_steps, world)
     flags = g.attn_flags() | g.topk_flags()
     ablation = fusion_ablation(g, P, stream, max(10, min(args.steps, 500)))
+    append = kv_append_timing(g, w, P, stream, max(10, min(args.steps, 500)))
 
     if rank != 0:
         if world > 1:
@@ -489,7 +539,8 @@ def run_gpu(args):
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "verify_requests": int(w.V), "draft_requests": int(w.B - w.V),
                    "heads": f"{w.Hq}q/{w.Hkv}kv", "head_dim": int(w.D), "k": int(w.k),
-                   "l2": "inputs larger than L2 (KV read per step %.0f MB)" % (ab["kv"] / 1e6)},
+                   "l2": "inputs larger than L2 (KV read per step %.0f MB), %d layers' pools rotated"
+                         % (ab["kv"] / 1e6, n_layers)},
         "attn_us": attn_ms * 1e3, "topk_us": topk_ms * 1e3,
         "kv_read_gbs": kv_gbs, "kv_read_frac_of_peak": kv_gbs / peak,
         "kv_read_frac_of_nominal": kv_gbs / NOMINAL_HBM_GBS,
@@ -507,6 +558,10 @@ def run_gpu(args):
                             "or next step's compute",
                 "serial_value": serial_us},
         "fusion_ablation": ablation,
+        "kv_append": append,
+        "layers": {"pools": n_layers, "bytes_per_layer": layer_bytes,
+                   "rotation": "step i reads layer i mod pools: its own K/V pools (the same rows at other "
+                               "addresses) and logit/LSE buffers"},
         "gpu_launches": 5 * args.steps,
         "breakdown_steps": nb,
         "clocks": clk,

@@ -309,6 +309,58 @@ def test_topk_budget_edges_and_ties():
     compare_topk(ni, nc, ref, [L] * V, [2, 0, 64], Hkv)
 
 
+def test_topk_skips_bad_group_map_and_negative_lengths():
+    """A verify request whose group_map entry names no request of the batch,
+    and one whose length is negative, are skipped (next_cnt 0) and flagged;
+    each counts as length 0 in the logit offsets of the requests after it, so
+    the valid request's lists are exact against the oracle."""
+    import sparse_self_speculative_pillar_gb300 as P
+    Hq, Hkv, k, L, K = 4, 2, 2, 300, 17
+    rng = np.random.default_rng(41)
+    lg = rng.standard_normal((1, Hq, k + 1, L)).astype(np.float32)
+    lse = np.log(np.exp(lg.astype(np.float64)).sum(-1)).astype(np.float32)
+    V = 3
+    shape = P.make_shape(B=3, Hq=Hq, Hkv=Hkv, D=64, k=k, max_sparse=1, max_len=L, num_slots=1, max_topk=K)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    lse_all = np.zeros((V, Hq, k + 1), np.float32)
+    lse_all[0] = lse[0]
+    nidx = torch.full((V, Hkv, K), -1, dtype=torch.int32, device="cuda")
+    ncnt = torch.full((V, Hkv), -1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(P.pillar_topk_workspace_bytes(shape, V), dtype=torch.uint8, device="cuda")
+    P.pillar_topk_select(shape, V, dev(lg.ravel()), dev(lse_all), dev(np.array([L, 280, -5], np.int32)),
+                         dev(np.array([0, 9, 2], np.int32)), dev(np.array([K, K, K], np.int32)), nidx, ncnt, ws)
+    assert P.pillar_get_error(ws) & P.FLAG_REQUEST
+    ni, nc = nidx.cpu().numpy(), ncnt.cpu().numpy()
+    assert np.all(nc[1] == 0) and np.all(nc[2] == 0)
+    ref = oracle.topk_select(Hq=Hq, Hkv=Hkv, k=k, row_lo=1, row_hi=k + 1, logits=lg.ravel().astype(np.float64),
+                             lse=lse.astype(np.float64), L=[L], K=[K], max_topk=K)
+    compare_topk(ni[:1], nc[:1], ref, [L], [K], Hkv)
+
+
+def test_verify_shorter_than_its_rows_gives_finite_topk():
+    """A verify request with L < k+1 is flagged but computed: its first rows
+    see no position (LSE -inf, every logit -inf).  Averaging those rows too,
+    the Top-K scores stay finite (such rows contribute 0, as in the oracle)
+    and the lists match the oracle's on the same dump."""
+    w = W.generate(W.scaled("qwen3_8b", B=4, length_scale=0.03, seed_offset=42, mode_rule="explicit",
+                            explicit_modes=(0, 1, 0, 1), explicit_phases=(1, 0, 2, 0)))
+    w.req_len[3] = w.k  # the last request: a verify with k positions for its k+1 rows
+    Lv = w.verify_len.astype(np.int64)
+    w.topk_K = np.clip(-(-Lv * w.recipe.s_num // w.recipe.s_den), 1, Lv).astype(np.int32)
+    g = Gpu(w, row_lo=0)  # average every row, the empty ones included
+    g.attn()
+    assert g.attn_flags() & 4
+    g.topk()
+    assert g.topk_flags() == 0
+    res = g.host()
+    lse = res["lse"][:w.V]
+    assert np.isneginf(lse[1][:, 0]).all()  # row 0 of the short request saw nothing
+    t = oracle.topk_select(Hq=w.Hq, Hkv=w.Hkv, k=w.k, row_lo=0, row_hi=w.k + 1, logits=res["logits"], lse=lse,
+                           L=w.verify_len, K=w.topk_K, max_topk=g.shape.max_topk)
+    assert np.isfinite(t.scores).all()
+    compare_topk(res["next_idx"], res["next_cnt"], t, w.verify_len, w.topk_K, w.Hkv)
+
+
 @pytest.mark.parametrize("L,K,n_tied", [(50000, 2500, 0), (12000, 3000, 6000), (45000, 2000, 5000)])
 def test_topk_long_rows_and_wide_ties(L, K, n_tied):
     """Rows longer than the select's shared-memory key buffer (keys stay in
