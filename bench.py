@@ -352,6 +352,71 @@ def kv_append_timing(g, w, P, stream, n):
             "calls": n, "flags": int(dflag.item())}
 
 
+def draft_slots_timing(g, w, P, stream, n):
+    """The draft lists with their pool slots already translated (as
+    pillar_draft_lists writes them after a verify step's Top-K): the attention
+    call through pillar_attn_unified_slotted against pillar_attn_unified on the
+    same lists, n calls each, out compared bit for bit; and pillar_draft_lists
+    itself on this step's Top-K (each verify request one token further on)."""
+    import torch
+    from workloads.device import to_device
+    kvo = w.kv_off
+    ss = np.zeros_like(w.sparse_idx)
+    for b in np.nonzero(w.req_mode == 0)[0]:
+        for h in range(w.Hkv):
+            c = int(w.sparse_cnt[b, h])
+            ss[b, h, :c] = w.slot_table[kvo[b] + w.sparse_idx[b, h, :c]]
+    ss_d = to_device(ss.astype(np.int32))
+
+    def call(slotted):
+        args = (g.shape, g.q, g.k_pool, g.v_pool, g.slot_table, g.req_mode, g.req_len, g.sparse_idx, g.sparse_cnt)
+        if slotted:
+            P.pillar_attn_unified_slotted(*args, ss_d, g.out, g.logits, g.lse, g.ws, stream=stream)
+        else:
+            P.pillar_attn_unified(*args, g.out, g.logits, g.lse, g.ws, stream=stream)
+
+    res = {"calls": n}
+    outs = {}
+    for name, slotted in (("positions", False), ("slotted", True)):
+        for _ in range(3):
+            call(slotted)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            call(slotted)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name + "_attn_us"] = e0.elapsed_time(e1) * 1e3 / n
+        outs[name] = g.out.clone()
+    res["same_out"] = bool(torch.equal(outs["positions"], outs["slotted"]))
+    res["slotted_vs_positions"] = res["slotted_attn_us"] / res["positions_attn_us"]
+    if w.V:
+        max_sparse = max(w.max_sparse, g.shape.max_topk + w.k)
+        shape = P.make_shape(B=w.B, Hq=w.Hq, Hkv=w.Hkv, D=w.D, k=w.k, max_sparse=max_sparse,
+                             max_len=g.shape.max_len, num_slots=w.num_slots, max_topk=g.shape.max_topk)
+        si = torch.zeros((w.B, w.Hkv, max_sparse), dtype=torch.int32, device="cuda")
+        sc = torch.zeros((w.B, w.Hkv), dtype=torch.int32, device="cuda")
+        sl = torch.zeros_like(si)
+        lv = to_device((w.verify_len - 1).astype(np.int32))  # each verify request one token further on
+        flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+        def lists():
+            P.pillar_draft_lists(shape, w.V, g.next_idx, g.next_cnt, g.group_map, lv, g.req_len, g.slot_table,
+                                 si, sc, sl, flags, stream=stream)
+
+        for _ in range(3):
+            lists()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            lists()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res["draft_lists_us"] = e0.elapsed_time(e1) * 1e3 / n
+        res["draft_lists_flags"] = int(flags.item())
+    return res
+
+
 def run_gpu(args):
     import torch
     import sparse_self_speculative_pillar_gb300 as P
@@ -515,6 +580,7 @@ def run_gpu(args):
     flags = g.attn_flags() | g.topk_flags()
     ablation = fusion_ablation(g, P, stream, max(10, min(args.steps, 500)))
     append = kv_append_timing(g, w, P, stream, max(10, min(args.steps, 500)))
+    slots = draft_slots_timing(g, w, P, stream, max(10, min(args.steps, 500)))
 
     if rank != 0:
         if world > 1:
@@ -559,6 +625,7 @@ def run_gpu(args):
                 "serial_value": serial_us},
         "fusion_ablation": ablation,
         "kv_append": append,
+        "draft_slots": slots,
         "layers": {"pools": n_layers, "bytes_per_layer": layer_bytes,
                    "rotation": "step i reads layer i mod pools: its own K/V pools (the same rows at other "
                                "addresses) and logit/LSE buffers"},

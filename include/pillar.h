@@ -170,6 +170,30 @@ PILLAR_API int pillar_attn_unified(const pillar_shape_t *shape, const uint16_t *
                         size_t ws_bytes, void *stream);
 
 /*
+ * pillar_attn_unified_slotted -- pillar_attn_unified whose draft lists come
+ * with their pool slots already translated (as pillar_draft_lists writes
+ * them), so that a draft key's K/V rows are reached without the dependent
+ * slot-table load ("SparseSpec-MLSys26", Unified batch scheduler + fused
+ * attention kernel: page size 1 -- every listed position is one slot).
+ *
+ *   sparse_slot  [B, Hkv, max_sparse] int32, device memory, 4-byte aligned,
+ *                or NULL (then exactly pillar_attn_unified): entry i of
+ *                request b's list of KV head h is the slot of position
+ *                sparse_idx[b, h, i], i.e. slot_table[off_b + that position].
+ *                The positions are still read: one outside [0, L_b) is
+ *                skipped and flagged (PILLAR_FLAG_INDEX), and a slot outside
+ *                [0, num_slots) is skipped and flagged (PILLAR_FLAG_SLOT).
+ *                Verify requests use slot_table as before.
+ * All other arguments, results and return codes as pillar_attn_unified.
+ */
+PILLAR_API int pillar_attn_unified_slotted(const pillar_shape_t *shape, const uint16_t *q, const uint16_t *k_pool,
+                                           const uint16_t *v_pool, const int32_t *slot_table,
+                                           const int32_t *req_mode, const int32_t *req_len,
+                                           const int32_t *sparse_idx, const int32_t *sparse_cnt,
+                                           const int32_t *sparse_slot, uint16_t *out, float *verify_logits,
+                                           float *verify_lse, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * pillar_topk_workspace_bytes -- workspace of pillar_topk_select for V
  * verify requests of length <= max_len.  Returns PILLAR_OK or PILLAR_ERR_ARG
  * (a bad shape, V < 0, or V * Hkv * max_len fp32 scores past 2^50 bytes).
@@ -245,6 +269,51 @@ PILLAR_API int pillar_topk_select_noalloc(const pillar_shape_t *shape, int32_t V
                                           const float *verify_lse, const int32_t *req_len,
                                           const int32_t *group_map, const int32_t *K, int32_t *next_idx,
                                           int32_t *next_cnt, int32_t *device_flags, void *stream);
+
+/*
+ * pillar_draft_lists -- the critical lists of a draft step that follows a
+ * verify step ("SparseSpec-MLSys26", 核心方法 / PillarAttn: the Top-K of the
+ * verify step is the critical set of the next k draft steps; the tokens
+ * appended since the verify step are attended as well).
+ *
+ * For verify request v of the earlier step, b = group_map[v] is its row in
+ * the draft step's batch and p = req_len[b] - verify_len[v] the tokens it has
+ * appended since; for every KV head h the kernel writes
+ *   sparse_idx[b, h, :] = next_idx[v, h, :next_cnt[v, h]],
+ *                         then verify_len[v], ..., verify_len[v] + p - 1
+ *   sparse_cnt[b, h]    = next_cnt[v, h] + p
+ * (ascending: the Top-K positions all lie below verify_len[v]), and with
+ * sparse_slot non-NULL, sparse_slot[b, h, i] = slot_table[off_b + that
+ * position], off_b = sum over b' < b of max(req_len[b'], 0), for
+ * pillar_attn_unified_slotted.  Rows of other requests are left untouched.
+ *
+ *   V              number of verify requests (host value).
+ *   next_idx,
+ *   next_cnt       [V, Hkv, max_topk], [V, Hkv] int32 as pillar_topk_select
+ *                  wrote them (shape->max_topk is the row stride).
+ *   group_map      [V] int32: batch index of request v in the draft step.
+ *   verify_len     [V] int32: request v's length at its verify step.
+ *   req_len        [B] int32: the draft step's lengths (shape->B requests).
+ *   slot_table     the draft step's slot table (needed with sparse_slot).
+ *   sparse_idx,
+ *   sparse_cnt,
+ *   sparse_slot    the draft step's lists: [B, Hkv, max_sparse] (stride
+ *                  shape->max_sparse), [B, Hkv], [B, Hkv, max_sparse] or NULL.
+ *   device_flags   NULL or a device int32 the kernel OR-s flags into:
+ *                  PILLAR_FLAG_REQUEST for a group_map entry outside [0, B)
+ *                  or a length that shrank since the verify step (no list is
+ *                  written; sparse_cnt 0 for the latter), PILLAR_FLAG_COUNT
+ *                  for a list longer than max_sparse (cut to max_sparse) or a
+ *                  next_cnt outside [0, max_topk] (clamped), PILLAR_FLAG_INDEX
+ *                  / PILLAR_FLAG_SLOT for a position or slot out of range
+ *                  (slot -1 written).
+ * All arrays are device memory, 4-byte aligned.  Asynchronous on `stream`;
+ * allocates nothing.  Returns PILLAR_OK, PILLAR_ERR_ARG or PILLAR_ERR_CUDA.
+ */
+PILLAR_API int pillar_draft_lists(const pillar_shape_t *shape, int32_t V, const int32_t *next_idx,
+                                  const int32_t *next_cnt, const int32_t *group_map, const int32_t *verify_len,
+                                  const int32_t *req_len, const int32_t *slot_table, int32_t *sparse_idx,
+                                  int32_t *sparse_cnt, int32_t *sparse_slot, int32_t *device_flags, void *stream);
 
 /*
  * pillar_get_error -- synchronises `stream`, then copies the device error

@@ -29,8 +29,8 @@ from . import _build
 
 __all__ = [
     "PillarShape", "make_shape", "PillarError", "load", "library_path", "build",
-    "pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_topk_workspace_bytes",
-    "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string",
+    "pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_attn_unified_slotted", "pillar_draft_lists",
+    "pillar_topk_workspace_bytes", "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string",
     "FLAG_INDEX", "FLAG_SLOT", "FLAG_REQUEST", "FLAG_COUNT", "FLAG_TIMEOUT", "FLAG_TOPK",
     "SCHEDULE_UNIFIED", "SCHEDULE_DRAFT_ONLY", "SCHEDULE_VERIFY_ONLY", "SCHEDULE_UNIFORM_ROWS",
     "pillar_kv_append", "PillarBuckets", "pillar_buckets_init", "pillar_buckets_admit", "pillar_buckets_retire", "pillar_buckets_step",
@@ -39,7 +39,8 @@ __all__ = [
 FLAG_INDEX, FLAG_SLOT, FLAG_REQUEST, FLAG_COUNT, FLAG_TIMEOUT, FLAG_TOPK = 1, 2, 4, 8, 16, 32
 # values of PillarShape.schedule (PILLAR_SCHEDULE_* in the header)
 SCHEDULE_UNIFIED, SCHEDULE_DRAFT_ONLY, SCHEDULE_VERIFY_ONLY, SCHEDULE_UNIFORM_ROWS = 0, 1, 2, 3
-EXPORTED = ("pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_topk_workspace_bytes",
+EXPORTED = ("pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_attn_unified_slotted",
+            "pillar_draft_lists", "pillar_topk_workspace_bytes",
             "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string",
             "pillar_kv_append", "pillar_buckets_init", "pillar_buckets_admit", "pillar_buckets_retire",
             "pillar_buckets_step")
@@ -107,6 +108,8 @@ def load():
     SP = ctypes.POINTER(PillarShape)
     lib.pillar_attn_workspace_bytes.argtypes = [SP, ctypes.POINTER(ctypes.c_size_t)]
     lib.pillar_attn_unified.argtypes = [SP] + [P] * 11 + [P, ctypes.c_size_t, P]
+    lib.pillar_attn_unified_slotted.argtypes = [SP] + [P] * 12 + [P, ctypes.c_size_t, P]
+    lib.pillar_draft_lists.argtypes = [SP, ctypes.c_int32] + [P] * 11
     lib.pillar_topk_workspace_bytes.argtypes = [SP, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]
     lib.pillar_topk_select.argtypes = [SP, ctypes.c_int32] + [P] * 7 + [P, ctypes.c_size_t, P]
     lib.pillar_topk_select_noalloc.argtypes = [SP, ctypes.c_int32] + [P] * 8 + [P]
@@ -182,6 +185,27 @@ def pillar_attn_unified(shape, q, k_pool, v_pool, slot_table, req_mode, req_len,
         ws_bytes if ws_bytes is not None else _nbytes(workspace), _stream(stream))
     if st:
         raise PillarError("pillar_attn_unified", st)
+
+
+def pillar_attn_unified_slotted(shape, q, k_pool, v_pool, slot_table, req_mode, req_len, sparse_idx, sparse_cnt,
+                                sparse_slot, out, verify_logits, verify_lse, workspace, stream=None, ws_bytes=None):
+    st = load().pillar_attn_unified_slotted(
+        ctypes.byref(shape), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(slot_table), _ptr(req_mode), _ptr(req_len),
+        _ptr(sparse_idx), _ptr(sparse_cnt), _ptr(sparse_slot), _ptr(out), _ptr(verify_logits), _ptr(verify_lse),
+        _ptr(workspace), ws_bytes if ws_bytes is not None else _nbytes(workspace), _stream(stream))
+    if st:
+        raise PillarError("pillar_attn_unified_slotted", st)
+
+
+def pillar_draft_lists(shape, V, next_idx, next_cnt, group_map, verify_len, req_len, slot_table, sparse_idx,
+                       sparse_cnt, sparse_slot=None, device_flags=None, stream=None):
+    """The draft step's lists (and, with sparse_slot, their slots) from a verify step's Top-K."""
+    st = load().pillar_draft_lists(
+        ctypes.byref(shape), int(V), _ptr(next_idx), _ptr(next_cnt), _ptr(group_map), _ptr(verify_len),
+        _ptr(req_len), _ptr(slot_table), _ptr(sparse_idx), _ptr(sparse_cnt), _ptr(sparse_slot), _ptr(device_flags),
+        _stream(stream))
+    if st:
+        raise PillarError("pillar_draft_lists", st)
 
 
 def pillar_topk_workspace_bytes(shape: PillarShape, V: int) -> int:

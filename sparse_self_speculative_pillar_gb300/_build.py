@@ -13,7 +13,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libpillar_gb300.so")
 SOURCES = ["pillar_plan.cu", "pillar_attn.cu", "pillar_topk.cu", "pillar_api.cu", "pillar_topk_noalloc.cu",
-           "pillar_sched.cu", "pillar_kv.cu"]
+           "pillar_sched.cu", "pillar_kv.cu", "pillar_lists.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

@@ -10,6 +10,7 @@
 
 #include "pillar_internal.h"
 #include "pillar_kv.h"
+#include "pillar_lists.h"
 
 namespace pillar {
 
@@ -104,6 +105,16 @@ int pillar_attn_unified(const pillar_shape_t *shape, const uint16_t *q, const ui
                         const int32_t *req_len, const int32_t *sparse_idx, const int32_t *sparse_cnt,
                         uint16_t *out, float *verify_logits, float *verify_lse, void *workspace,
                         size_t ws_bytes, void *stream) {
+    return pillar_attn_unified_slotted(shape, q, k_pool, v_pool, slot_table, req_mode, req_len, sparse_idx,
+                                       sparse_cnt, nullptr, out, verify_logits, verify_lse, workspace, ws_bytes,
+                                       stream);
+}
+
+int pillar_attn_unified_slotted(const pillar_shape_t *shape, const uint16_t *q, const uint16_t *k_pool,
+                                const uint16_t *v_pool, const int32_t *slot_table, const int32_t *req_mode,
+                                const int32_t *req_len, const int32_t *sparse_idx, const int32_t *sparse_cnt,
+                                const int32_t *sparse_slot, uint16_t *out, float *verify_logits,
+                                float *verify_lse, void *workspace, size_t ws_bytes, void *stream) {
     int st = check_shape(shape);
     if (st != PILLAR_OK) return st;
     const pillar_shape_t &s = *shape;
@@ -122,8 +133,10 @@ int pillar_attn_unified(const pillar_shape_t *shape, const uint16_t *q, const ui
     // everything else is read or written in 4-byte words
     if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 4) ||
         !aligned(verify_logits, 8) || !aligned(verify_lse, 4) || !aligned(slot_table, 4) || !aligned(req_mode, 4) ||
-        !aligned(req_len, 4) || !aligned(sparse_cnt, 4) || (sparse_idx && !aligned(sparse_idx, 4)))
+        !aligned(req_len, 4) || !aligned(sparse_cnt, 4) || (sparse_idx && !aligned(sparse_idx, 4)) ||
+        (sparse_slot && !aligned(sparse_slot, 4)))
         return PILLAR_ERR_ARG;
+    if (sparse_slot && !sparse_idx) return PILLAR_ERR_ARG;
     const AttnLayout lay = attn_layout(s);
     if (!workspace || !aligned(workspace, 256) || ws_bytes < lay.total) return PILLAR_ERR_WORKSPACE;
     const int nsm = sm_count();
@@ -155,6 +168,7 @@ int pillar_attn_unified(const pillar_shape_t *shape, const uint16_t *q, const ui
     aa.v_pool = v_pool;
     aa.slot_table = slot_table;
     aa.sparse_idx = sparse_idx;
+    aa.sparse_slot = sparse_slot;
     aa.out = out;
     aa.logits = verify_logits;
     aa.lse = verify_lse;
@@ -252,6 +266,42 @@ int pillar_kv_append(const pillar_shape_t *shape, const uint16_t *k_new, const u
     a.Hkv = shape->Hkv;
     a.D = shape->D;
     return launch_kv_append(a, nsm, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PILLAR_OK : PILLAR_ERR_CUDA;
+}
+
+int pillar_draft_lists(const pillar_shape_t *shape, int32_t V, const int32_t *next_idx, const int32_t *next_cnt,
+                       const int32_t *group_map, const int32_t *verify_len, const int32_t *req_len,
+                       const int32_t *slot_table, int32_t *sparse_idx, int32_t *sparse_cnt, int32_t *sparse_slot,
+                       int32_t *device_flags, void *stream) {
+    const int st = check_shape(shape);
+    if (st != PILLAR_OK) return st;
+    if (V < 0 || V > 65535 * 32) return PILLAR_ERR_ARG;
+    if (V == 0) return PILLAR_OK;
+    if (!next_idx || !next_cnt || !group_map || !verify_len || !req_len || !sparse_idx || !sparse_cnt)
+        return PILLAR_ERR_ARG;
+    if (shape->max_sparse < 1 || (sparse_slot && !slot_table)) return PILLAR_ERR_ARG;
+    for (const void *ptr : {(const void *)next_idx, (const void *)next_cnt, (const void *)group_map,
+                            (const void *)verify_len, (const void *)req_len, (const void *)slot_table,
+                            (const void *)sparse_idx, (const void *)sparse_cnt, (const void *)sparse_slot,
+                            (const void *)device_flags})
+        if (!aligned(ptr, 4)) return PILLAR_ERR_ARG;  // 4-byte words throughout
+    ListsArgs a;
+    a.next_idx = next_idx;
+    a.next_cnt = next_cnt;
+    a.group_map = group_map;
+    a.verify_len = verify_len;
+    a.req_len = req_len;
+    a.slot_table = slot_table;
+    a.sparse_idx = sparse_idx;
+    a.sparse_cnt = sparse_cnt;
+    a.sparse_slot = sparse_slot;
+    a.flags = device_flags;
+    a.num_slots = shape->num_slots;
+    a.V = V;
+    a.B = shape->B;
+    a.Hkv = shape->Hkv;
+    a.max_topk = shape->max_topk;
+    a.max_sparse = shape->max_sparse;
+    return launch_draft_lists(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PILLAR_OK : PILLAR_ERR_CUDA;
 }
 
 int pillar_get_error(void *workspace, void *stream, int32_t *flags) {

@@ -66,6 +66,7 @@ struct AttnParams {
     CUtensorMap tmap_k, tmap_v;  // the pools as [num_slots * Hkv rows, D] bf16, box 64 x 1, 128-byte swizzle
     const uint16_t *q, *k_pool, *v_pool;
     const int *slot_table, *sparse_idx;
+    const int *sparse_slot;  // null, or the draft lists' slots (same layout as sparse_idx)
     uint16_t *out;
     float *logits, *lse;
     WsHeader *hdr;
@@ -249,7 +250,11 @@ __device__ void resolver(const AttnParams &p, const Ctx &c, int lane) {
         const long long lgo = p.logit_off[b];
         const bool verify = ri.mode == 1;
         const int n = itm.end - itm.begin;
-        const int *list = p.sparse_idx + ((long long)b * p.Hkv + g) * p.max_sparse + itm.begin;
+        const long long lrow = ((long long)b * p.Hkv + g) * p.max_sparse + itm.begin;
+        const int *list = p.sparse_idx + lrow;
+        // draft lists with their slots already translated: the slot is read beside the position
+        // instead of through the slot table (one round trip instead of two dependent ones)
+        const int *slist = (!verify && p.sparse_slot) ? p.sparse_slot + lrow : nullptr;
         int *rows = c.rowlist + rb * kMaxChunk;
         int bad = 0;
         // 16 independent loads per lane keep the dependent list -> slot chain short
@@ -259,13 +264,15 @@ __device__ void resolver(const AttnParams &p, const Ctx &c, int lane) {
             for (int r = 0; r < 16; ++r) {
                 const int i = base + r * 32 + lane;
                 pos[r] = i < n ? (verify ? itm.begin + i : __ldg(list + i)) : -1;
+                if (slist) slot[r] = i < n ? __ldg(slist + i) : -1;
             }
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 const int i = base + r * 32 + lane;
                 const bool inpos = pos[r] >= 0 && pos[r] < ri.len;
                 if (i < n && !inpos) bad |= PILLAR_FLAG_INDEX;
-                slot[r] = (i < n && inpos) ? __ldg(p.slot_table + kvo + pos[r]) : -1;
+                if (!slist) slot[r] = (i < n && inpos) ? __ldg(p.slot_table + kvo + pos[r]) : -1;
+                else if (!inpos) slot[r] = -1;
             }
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
@@ -1178,6 +1185,7 @@ cudaError_t launch_attn(const AttnArgs &a, int nsm, cudaStream_t st) {
     p.v_pool = a.v_pool;
     p.slot_table = a.slot_table;
     p.sparse_idx = a.sparse_idx;
+    p.sparse_slot = a.sparse_slot;
     p.out = a.out;
     p.logits = a.logits;
     p.lse = a.lse;

@@ -143,6 +143,7 @@ cudaError_t launch_plan(const PlanArgs &a, cudaStream_t st);
 struct AttnArgs {
     const uint16_t *q, *k_pool, *v_pool;
     const int *slot_table, *sparse_idx;
+    const int *sparse_slot;  // null, or the slots of the draft lists (layout of sparse_idx)
     uint16_t *out;
     float *logits, *lse;
     char *ws;
