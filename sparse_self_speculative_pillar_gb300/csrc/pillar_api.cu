@@ -226,7 +226,8 @@ int pillar_topk_select(const pillar_shape_t *shape, int32_t V, const float *veri
     ta.next_idx = next_idx;
     ta.next_cnt = next_cnt;
     ta.ws = static_cast<char *>(workspace);
-    ta.scores = reinterpret_cast<float *>(ta.ws + topk_scores_offset());
+    ta.rows = reinterpret_cast<TopkRow *>(ta.ws + topk_rows_offset());
+    ta.scores = reinterpret_cast<float *>(ta.ws + topk_scores_offset(V));
     ta.B = shape->B;
     ta.V = V;
     ta.Hq = shape->Hq;

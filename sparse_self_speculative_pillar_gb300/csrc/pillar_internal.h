@@ -121,10 +121,18 @@ inline AttnLayout attn_layout(const pillar_shape_t &s) {
     return l;
 }
 
-// Top-K workspace: header (error word) + packed scores [V][Hkv][L_v].
-inline size_t topk_scores_offset() { return sizeof(WsHeader); }
+// Top-K workspace: header (error word), one record per verify request (what
+// the score pass found out about it, for the select), then the packed scores
+// [V][Hkv][L_v].
+struct TopkRow {
+    int L;            // L_v, or -1 when the request is skipped
+    int K;            // its budget as given
+    long long sc_off; // offset of its scores [Hkv][L_v] in the scores scratch
+};
+inline size_t topk_rows_offset() { return sizeof(WsHeader); }
+inline size_t topk_scores_offset(int V) { return align256(sizeof(WsHeader) + sizeof(TopkRow) * (size_t)V); }
 inline size_t topk_ws_bytes(const pillar_shape_t &s, int V) {
-    return align256(sizeof(WsHeader) + sizeof(float) * (size_t)V * s.Hkv * (size_t)s.max_len);
+    return align256(topk_scores_offset(V) + sizeof(float) * (size_t)V * s.Hkv * (size_t)s.max_len);
 }
 
 // ------------------------------------------------------------------ launchers
@@ -161,6 +169,7 @@ struct TopkArgs {
     const int *req_len, *group_map, *K;
     int *next_idx, *next_cnt;
     char *ws;
+    TopkRow *rows;
     float *scores;
     int B, V, Hq, Hkv, k, row_lo, row_hi, max_topk, max_len;
 };

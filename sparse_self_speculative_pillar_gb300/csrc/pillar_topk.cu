@@ -13,11 +13,16 @@
 //      every (verify request, KV head), 2048 positions per CTA, coalesced
 //      loads; writes fp32 scores (scratch in the workspace, L2-resident for
 //      the next kernel at the usual sizes).
-//   2. topk_select: one CTA per (verify request, KV head): 4-pass 8-bit radix
-//      select of the K-th largest score on the order-preserving uint32 key
-//      of the (non-negative) fp32 score, then an ordered compaction that
-//      keeps everything above the threshold plus the lowest positions equal
-//      to it -- the output comes out ascending with no sort.
+//   2. topk_select: one CTA per (verify request, KV head): the K-th largest
+//      score, on the order-preserving uint32 key of the (non-negative) fp32
+//      score, by a radix select whose first digit is the key's top 11 bits
+//      (exponent and three mantissa bits), histogrammed while the keys are
+//      loaded; the keys of the bucket that holds the K-th largest are then
+//      gathered and the two remaining 10-bit digits are resolved on them alone
+//      (a byte-wise radix select over every key stands in when that bucket is
+//      too large to gather).  An ordered compaction then keeps everything
+//      above the threshold plus the lowest positions equal to it -- the output
+//      comes out ascending with no sort.
 // The two are chained by programmatic dependent launch: the select grid is
 // scheduled while the scores finish and waits for them before reading.
 #include "pillar_device.cuh"
@@ -29,6 +34,7 @@ struct TopkParams {
     const int *req_len, *group_map, *K;
     int *next_idx, *next_cnt;
     WsHeader *hdr;
+    TopkRow *rows;
     float *scores;
     int B, V, Hq, Hkv, G, k, row_lo, row_hi, max_topk, max_len, smem_keys;
 };
@@ -47,6 +53,13 @@ constexpr int kScoreChunk = kScoreThreads * kScorePerThread;
 constexpr int kSelectThreads = 1024;
 constexpr int kSelectSmemKeys = 40 * 1024;  // keys kept in shared memory (160 KB); longer rows stay in global
 constexpr int kSelectWarps = kSelectThreads / 32;
+constexpr int kCoarseShift = 20;                   // first digit: key bits 30..20
+constexpr int kCoarseBins = 1 << (31 - kCoarseShift);
+constexpr int kFineBins = 1 << 10;                 // then bits 19..10 and 9..0
+constexpr int kCandCap = 4096;                     // keys of the first digit's bucket kept for the fine digits
+// shared memory after the keys: coarse histogram, two fine histograms, candidates, per-warp byte histograms
+constexpr size_t kSelectScratchBytes =
+    sizeof(uint32_t) * (kCoarseBins + 2 * kFineBins + kCandCap + kSelectWarps * 256);
 
 // Offsets of verify request v in the packed logits (sums over v' < v of
 // Hq*(k+1)*max(L_v', 0), the offsets the attention planner gives the dump)
@@ -118,13 +131,17 @@ __global__ void __launch_bounds__(kScoreThreads) topk_scores_kernel(const TopkPa
     const int v = blockIdx.z, g = blockIdx.y;
     const int L = verify_len(p, v);
     const int t0 = blockIdx.x * kScoreChunk;
+    const bool recorder = blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0;  // writes the request's record
     if (L < 0 || L > p.max_len) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&p.hdr->err, PILLAR_FLAG_REQUEST);
+        if (recorder) p.rows[v] = TopkRow{-1, 0, 0};
         return;
     }
+    if (L == 0 && recorder) p.rows[v] = TopkRow{0, p.K[v], 0};
     if (t0 >= L) return;
     long long lg_off, sc_off;
     verify_offsets(p, v, &lg_off, &sc_off);
+    if (recorder) p.rows[v] = TopkRow{L, p.K[v], sc_off};
     const int R = p.row_hi - p.row_lo, nrows = R * p.G;
     const int nrows_pad = (nrows + kScoreRowBatch - 1) / kScoreRowBatch * kScoreRowBatch;
     // per averaged row: its offset in the logits and 24 - lse*log2(e); the
@@ -187,27 +204,158 @@ __device__ int2 select_block_scan2(int a, int b, int2 *total) {
 }
 
 __device__ __forceinline__ uint32_t score_key(float s) { return __float_as_uint(s) & 0x7fffffffu; }
+// The key of position t (rows too long for shared memory are read from the scores themselves).
+__device__ __forceinline__ uint32_t key_at(const uint32_t *keys, int t) { return keys[t] & 0x7fffffffu; }
 
-__global__ void __launch_bounds__(kSelectThreads, 1) topk_select_kernel(const TopkParams p) {
-    extern __shared__ uint32_t skeys[];
-    __shared__ uint32_t whist[kSelectWarps][256];  // one histogram per warp: no cross-warp atomics
+// The bin of hist[0, NB) that holds the rem-th largest key (rem >= 1, bins
+// walked from the top) and the key's rank inside that bin, found by the whole
+// block: thread i owns the NB/1024 bins below NB-1-i*NB/1024, a warp scan and a
+// scan of the 32 warp totals give every thread the count above its bins, and
+// the thread whose bins cross rem writes the results (read after the closing
+// barrier).  s_wsum: 32 words of scratch.
+template <int NB>
+__device__ __forceinline__ void block_find_bin(const uint32_t *hist, uint32_t rem, uint32_t *s_wsum, uint32_t *s_bin,
+                                               uint32_t *s_rank) {
+    constexpr int kPer = NB / kSelectThreads;
+    static_assert(kPer == 1 || kPer == 2, "bins per thread");
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int top = NB - 1 - tid * kPer;
+    uint32_t c[kPer];
+    if (kPer == 2) {  // the thread's two bins in one 8-byte load
+        const uint2 pr = *reinterpret_cast<const uint2 *>(hist + top - 1);
+        c[0] = pr.y;
+        c[kPer - 1] = pr.x;
+    } else {
+        c[0] = hist[top];
+    }
+    uint32_t sum = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) sum += c[j];
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_wsum[w] = incl;
+    __syncthreads();
+    const uint32_t ws = s_wsum[lane];
+    uint32_t wincl = ws;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, wincl, o);
+        if (lane >= o) wincl += y;
+    }
+    const uint32_t above_warp = __shfl_sync(0xffffffffu, wincl - ws, w);
+    uint32_t cum = above_warp + incl - sum;
+    if (cum < rem && cum + sum >= rem) {
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            if (cum + c[j] >= rem) {
+                *s_bin = (uint32_t)(top - j);
+                *s_rank = rem - cum;
+                break;
+            }
+            cum += c[j];
+        }
+    }
+    __syncthreads();
+}
+
+// Byte-wise radix select of the rem-th largest of L keys (every key visited in
+// each of four passes): the stand-in for a first-digit bucket too large to
+// gather.  Returns the key; *rank gets its rank among the keys equal to it.
+__device__ uint32_t radix_select_bytes(const uint32_t *keys, int L, uint32_t rem, uint32_t (*whist)[256],
+                                       uint32_t *rank) {
     __shared__ uint32_t hist[256];
     __shared__ uint32_t s_prefix, s_mask, s_remaining;
-    pdl_wait_prerequisites();  // the scores (and everything before them) are complete and visible
-    const int v = blockIdx.y, g = blockIdx.x, tid = threadIdx.x;
-    __shared__ int s_lk[2];
-    if (tid == 32) {  // the request's length and budget, read while warp 0 sums the offsets
-        s_lk[0] = verify_len(p, v);
-        s_lk[1] = p.K[v];
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        s_prefix = 0;
+        s_mask = 0;
+        s_remaining = rem;
     }
-    long long lg_off, sc_off;
-    verify_offsets(p, v, &lg_off, &sc_off);  // ends with a block barrier
-    const int L = s_lk[0];
+    __syncthreads();
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        uint32_t *myhist = whist[tid >> 5];
+        for (int i = tid & 31; i < 256; i += 32) myhist[i] = 0;
+        __syncwarp();
+        const uint32_t prefix = s_prefix, mask = s_mask;
+        for (int t = tid; t < L; t += blockDim.x) {
+            const uint32_t key = key_at(keys, t);
+            if ((key & mask) == prefix) atomicAdd(&myhist[(key >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (tid < 256) {
+            uint32_t c = 0;
+#pragma unroll 8
+            for (int w = 0; w < kSelectWarps; ++w) c += whist[w][tid];
+            hist[tid] = c;
+        }
+        __syncthreads();
+        if (tid < 32) {
+            const uint32_t r = s_remaining;
+            __syncwarp();  // every lane has read s_remaining before it changes
+            uint32_t bin = 0, rk = 0;
+            bool mine = false;
+            {
+                // (find_bin writes from one lane; the lane also updates the prefix)
+                constexpr int kPer = 8;
+                const int lane = tid, top = 255 - lane * kPer;
+                uint32_t sum = 0;
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) sum += hist[top - i];
+                uint32_t incl = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const uint32_t before = incl - sum;
+                if (before < r && incl >= r) {
+                    uint32_t cum = before;
+                    for (int i = 0; i < kPer; ++i) {
+                        const uint32_t c = hist[top - i];
+                        if (cum + c >= r) {
+                            bin = (uint32_t)(top - i);
+                            rk = r - cum;
+                            mine = true;
+                            break;
+                        }
+                        cum += c;
+                    }
+                }
+            }
+            if (mine) {
+                s_prefix = prefix | (bin << shift);
+                s_mask = mask | (255u << shift);
+                s_remaining = rk;
+            }
+        }
+        __syncthreads();
+    }
+    *rank = s_remaining;
+    return s_prefix;
+}
+
+__global__ void __launch_bounds__(kSelectThreads, 1) topk_select_kernel(const TopkParams p) {
+    extern __shared__ uint32_t smem[];
+    uint32_t *skeys = smem;
+    uint32_t *coarse = smem + p.smem_keys;
+    uint32_t *fine_a = coarse + kCoarseBins, *fine_b = fine_a + kFineBins;
+    uint32_t *cand = fine_b + kFineBins;
+    uint32_t(*whist)[256] = reinterpret_cast<uint32_t(*)[256]>(cand + kCandCap);
+    __shared__ uint32_t s_bin, s_rank, s_ncand, s_wsum[kSelectWarps];
+    pdl_wait_prerequisites();  // the scores and the score pass's records are complete and visible
+    const int v = blockIdx.y, g = blockIdx.x, tid = threadIdx.x;
+    const TopkRow rec = p.rows[v];
+    const int L = rec.L;
     if (L < 0 || L > p.max_len) {
         if (tid == 0) p.next_cnt[v * p.Hkv + g] = 0;
         return;
     }
-    int K = s_lk[1];
+    int K = rec.K;
     K = K < 0 ? 0 : (K > L ? L : K);
     if (K > p.max_topk) {
         if (tid == 0) atomicOr(&p.hdr->err, PILLAR_FLAG_TOPK);
@@ -220,9 +368,14 @@ __global__ void __launch_bounds__(kSelectThreads, 1) topk_select_kernel(const To
         for (int t = tid; t < L; t += blockDim.x) dst[t] = t;
         return;
     }
-    const float *sc = p.scores + sc_off + (long long)g * L;
-    const uint32_t *keys;
-    if (L <= p.smem_keys) {
+    const float *sc = p.scores + rec.sc_off + (long long)g * L;
+    for (int i = tid; i < kCoarseBins; i += kSelectThreads) coarse[i] = 0;
+    for (int i = tid; i < 2 * kFineBins; i += kSelectThreads) fine_a[i] = 0;
+    if (tid == 0) s_ncand = 0;
+    __syncthreads();
+    // The keys (kept in shared memory when they fit) and the histogram of their first digit.
+    const bool in_smem = L <= p.smem_keys;
+    {
         constexpr int kU = 8;  // independent loads in flight per thread
         for (int t0 = 0; t0 < L; t0 += kU * kSelectThreads) {
             float x[kU];
@@ -234,92 +387,67 @@ __global__ void __launch_bounds__(kSelectThreads, 1) topk_select_kernel(const To
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 const int t = t0 + u * kSelectThreads + tid;
-                if (t < L) skeys[t] = score_key(x[u]);
-            }
-        }
-        keys = skeys;
-    } else {
-        keys = reinterpret_cast<const uint32_t *>(sc);  // signless already: scores are >= 0
-    }
-    if (tid == 0) {
-        s_prefix = 0;
-        s_mask = 0;
-        s_remaining = (uint32_t)K;
-    }
-    __syncthreads();
-
-    // Radix select, most significant byte first, of the K-th largest key.
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        uint32_t *myhist = whist[tid >> 5];
-        for (int i = tid & 31; i < 256; i += 32) myhist[i] = 0;
-        __syncwarp();
-        const uint32_t prefix = s_prefix, mask = s_mask;
-        for (int t = tid; t < L; t += blockDim.x) {
-            const uint32_t key = keys[t] & 0x7fffffffu;
-            if ((key & mask) == prefix) atomicAdd(&myhist[(key >> shift) & 255u], 1u);
-        }
-        __syncthreads();
-        if (tid < 256) {
-            uint32_t c = 0;
-#pragma unroll 8
-            for (int w = 0; w < kSelectWarps; ++w) c += whist[w][tid];
-            hist[tid] = c;
-        }
-        __syncthreads();
-        if (tid < 32) {
-            // lane l owns digits 255-8l .. 248-8l (descending)
-            const uint32_t rem = s_remaining;
-            uint32_t cnt[8], sum = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                cnt[i] = hist[255 - 8 * tid - i];
-                sum += cnt[i];
-            }
-            uint32_t incl = sum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (tid >= o) incl += y;
-            }
-            const uint32_t before = incl - sum;
-            const bool mine = before < rem && incl >= rem;
-            __syncwarp();  // every lane has read s_remaining before it changes
-            if (mine) {
-                uint32_t cum = before;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (cum + cnt[i] >= rem) {
-                        s_prefix = prefix | ((uint32_t)(255 - 8 * tid - i) << shift);
-                        s_mask = mask | (255u << shift);
-                        s_remaining = rem - cum;
-                        break;
-                    }
-                    cum += cnt[i];
+                if (t < L) {
+                    const uint32_t key = score_key(x[u]);
+                    if (in_smem) skeys[t] = key;
+                    atomicAdd(&coarse[key >> kCoarseShift], 1u);
                 }
             }
         }
-        __syncthreads();
     }
-    const uint32_t T = s_prefix;
-    const int need_eq = (int)s_remaining;
+    // (scores are >= 0: their keys need no sign fix)
+    const uint32_t *keys = in_smem ? skeys : reinterpret_cast<const uint32_t *>(sc);
+    __syncthreads();
+    block_find_bin<kCoarseBins>(coarse, (uint32_t)K, s_wsum, &s_bin, &s_rank);
+    const uint32_t b1 = s_bin, r1 = s_rank;
+    // Gather the keys of that bucket.
+    for (int t = tid; t < L; t += kSelectThreads) {
+        const uint32_t key = key_at(keys, t);
+        if ((key >> kCoarseShift) == b1) {
+            const uint32_t i = atomicAdd(&s_ncand, 1u);
+            if (i < (uint32_t)kCandCap) cand[i] = key;
+        }
+    }
+    __syncthreads();
+    const int ncand = (int)s_ncand;
+    uint32_t T;
+    int need_eq;
+    if (ncand <= kCandCap) {
+        // the two fine digits, on the candidates alone
+        for (int i = tid; i < ncand; i += kSelectThreads) atomicAdd(&fine_a[(cand[i] >> 10) & 1023u], 1u);
+        __syncthreads();
+        block_find_bin<kFineBins>(fine_a, r1, s_wsum, &s_bin, &s_rank);
+        const uint32_t b2 = s_bin, r2 = s_rank;
+        for (int i = tid; i < ncand; i += kSelectThreads) {
+            const uint32_t key = cand[i];
+            if (((key >> 10) & 1023u) == b2) atomicAdd(&fine_b[key & 1023u], 1u);
+        }
+        __syncthreads();  // (also: every thread has read s_bin and s_rank before they change)
+        block_find_bin<kFineBins>(fine_b, r2, s_wsum, &s_bin, &s_rank);
+        T = (b1 << kCoarseShift) | (b2 << 10) | s_bin;
+        need_eq = (int)s_rank;
+    } else {
+        uint32_t rk;
+        T = radix_select_bytes(keys, L, (uint32_t)K, whist, &rk);
+        need_eq = (int)rk;
+    }
 
-    // Ordered compaction: each thread owns a contiguous run of positions.
-    const int per = (L + blockDim.x - 1) / blockDim.x;
+    // Ordered compaction: each thread owns a contiguous run of positions (an odd run length, so
+    // that the 32 lanes of a warp read 32 different shared-memory banks).
+    const int per = ((L + blockDim.x - 1) / blockDim.x) | 1;
     const int tb = min(L, tid * per), te = min(L, tb + per);
     int cgt = 0, ceq = 0;
     for (int t = tb; t < te; ++t) {
-        const uint32_t key = keys[t] & 0x7fffffffu;
+        const uint32_t key = key_at(keys, t);
         cgt += key > T;
         ceq += key == T;
     }
     int2 tot;
     const int2 before = select_block_scan2(cgt, ceq, &tot);
-    const int gt_before = before.x, eq_before = before.y;
-    int out = gt_before + min(eq_before, need_eq);
-    int eq_rank = eq_before;
+    int out = before.x + min(before.y, need_eq);
+    int eq_rank = before.y;
     for (int t = tb; t < te; ++t) {
-        const uint32_t key = keys[t] & 0x7fffffffu;
+        const uint32_t key = key_at(keys, t);
         if (key > T) {
             dst[out++] = t;
         } else if (key == T) {
@@ -339,6 +467,7 @@ cudaError_t launch_topk_select(const TopkArgs &a, cudaStream_t st) {
     p.next_idx = a.next_idx;
     p.next_cnt = a.next_cnt;
     p.hdr = reinterpret_cast<WsHeader *>(a.ws);
+    p.rows = a.rows;
     p.scores = a.scores;
     p.B = a.B;
     p.V = a.V;
@@ -350,7 +479,7 @@ cudaError_t launch_topk_select(const TopkArgs &a, cudaStream_t st) {
     p.row_hi = a.row_hi;
     p.max_topk = a.max_topk;
     p.max_len = a.max_len;
-    p.smem_keys = min(a.max_len, kSelectSmemKeys);
+    p.smem_keys = min((a.max_len + 3) & ~3, kSelectSmemKeys);  // (a multiple of 4: the histograms after the keys are 16-byte aligned)
     if (p.V == 0) return cudaSuccess;
     // launch attributes, once per device context
     static unsigned long long configured[kMaxDevices] = {};
@@ -359,10 +488,10 @@ cudaError_t launch_topk_select(const TopkArgs &a, cudaStream_t st) {
     cudaError_t e = current_device_context(&dev, &ctx);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    const size_t sel_smem = sizeof(uint32_t) * (size_t)p.smem_keys;
+    const size_t sel_smem = sizeof(uint32_t) * (size_t)p.smem_keys + kSelectScratchBytes;
     if (ctx == 0 || __atomic_load_n(&configured[dev], __ATOMIC_ACQUIRE) != ctx) {
         e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(sizeof(uint32_t) * kSelectSmemKeys));
+                                 (int)(sizeof(uint32_t) * kSelectSmemKeys + kSelectScratchBytes));
         if (e != cudaSuccess) return e;
         e = current_device_context(&dev, &ctx);
         if (e != cudaSuccess) return e;

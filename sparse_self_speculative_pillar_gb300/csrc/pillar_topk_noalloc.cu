@@ -23,7 +23,7 @@ namespace {
 using namespace pillar;
 
 // The built-in scratch: the Top-K workspace layout (header with the error
-// word, then the packed scores [V][Hkv][max_len]) capped at
+// word, per-request records, then the packed scores [V][Hkv][max_len]) capped at
 // PILLAR_NOALLOC_SCRATCH_BYTES.  In host code this name is only a stand-in
 // for the device copy; the device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_topk_scratch[PILLAR_NOALLOC_SCRATCH_BYTES];
@@ -90,7 +90,8 @@ int pillar_topk_select_noalloc(const pillar_shape_t *shape, int32_t V, const flo
         ta.next_idx = next_idx;
         ta.next_cnt = next_cnt;
         ta.ws = ws;
-        ta.scores = reinterpret_cast<float *>(ws + topk_scores_offset());
+        ta.rows = reinterpret_cast<TopkRow *>(ws + topk_rows_offset());
+        ta.scores = reinterpret_cast<float *>(ws + topk_scores_offset(V));
         ta.B = shape->B;
         ta.V = V;
         ta.Hq = shape->Hq;
