@@ -282,16 +282,19 @@ def whole_job_us(max_elapsed_ms, steps, world):
 # --------------------------------------------------------------------------- GPU arm
 
 def fusion_ablation(g, P, stream, n):
-    """The attention call under the unified schedule and under the two
-    schedules it replaces ("SparseSpec-MLSys26", Unified batch scheduler +
-    fused attention kernel: a sequential pair of launches, and a joint batch
-    without per-mode dispatch), each timed over n calls on the launching
-    stream.  Every schedule writes the same outputs; `*_same_out` says whether
-    the out tensor came back bit for bit equal to the unified pass's."""
+    """The attention call under the unified schedule and under the schedules
+    it replaces ("SparseSpec-MLSys26", Unified batch scheduler + fused
+    attention kernel: a sequential pair of launches, and a naive joint batch;
+    uniform_rows is the joint batch with only the per-mode row layout taken
+    away), each timed over n calls on the launching stream.  Every schedule
+    computes the same outputs; `*_same_out` says whether the out tensor came
+    back bit for bit equal to the unified pass's (the naive joint batch splits
+    long contexts differently, so its rows agree within rounding only)."""
     import torch
     plans = (("unified", (P.SCHEDULE_UNIFIED,)),
              ("sequential", (P.SCHEDULE_DRAFT_ONLY, P.SCHEDULE_VERIFY_ONLY)),
-             ("uniform_rows", (P.SCHEDULE_UNIFORM_ROWS,)))
+             ("uniform_rows", (P.SCHEDULE_UNIFORM_ROWS,)),
+             ("naive_joint", (P.SCHEDULE_NAIVE_JOINT,)))
 
     def run(scheds):
         for sch in scheds:

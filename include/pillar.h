@@ -114,12 +114,19 @@ typedef struct pillar_shape {
  *                 the slots of one TMEM lane quadrant) instead of its own
  *                 spread of the G rows over the four quadrants: a joint batch
  *                 without per-mode dispatch.
+ *   NAIVE_JOINT   the naive joint batch: the UNIFORM_ROWS row layout for every
+ *                 request, work items of the largest size the pipeline takes
+ *                 (2048 keys, whatever verify_chunk and draft_chunk say), and
+ *                 no dynamic load balancing -- each CTA of the persistent grid
+ *                 takes the (request, KV head) units c, c + grid, c + 2 grid,
+ *                 ... in batch order and works through all of their items.
  * The device error word is cleared by every call; it reports that call only.
  */
 #define PILLAR_SCHEDULE_UNIFIED 0
 #define PILLAR_SCHEDULE_DRAFT_ONLY 1
 #define PILLAR_SCHEDULE_VERIFY_ONLY 2
 #define PILLAR_SCHEDULE_UNIFORM_ROWS 3
+#define PILLAR_SCHEDULE_NAIVE_JOINT 4
 
 /*
  * pillar_attn_workspace_bytes -- bytes of workspace pillar_attn_unified

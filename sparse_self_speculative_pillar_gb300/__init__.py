@@ -32,13 +32,13 @@ __all__ = [
     "pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_attn_unified_slotted", "pillar_draft_lists",
     "pillar_topk_workspace_bytes", "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string",
     "FLAG_INDEX", "FLAG_SLOT", "FLAG_REQUEST", "FLAG_COUNT", "FLAG_TIMEOUT", "FLAG_TOPK",
-    "SCHEDULE_UNIFIED", "SCHEDULE_DRAFT_ONLY", "SCHEDULE_VERIFY_ONLY", "SCHEDULE_UNIFORM_ROWS",
+    "SCHEDULE_UNIFIED", "SCHEDULE_DRAFT_ONLY", "SCHEDULE_VERIFY_ONLY", "SCHEDULE_UNIFORM_ROWS", "SCHEDULE_NAIVE_JOINT",
     "pillar_kv_append", "PillarBuckets", "pillar_buckets_init", "pillar_buckets_admit", "pillar_buckets_retire", "pillar_buckets_step",
 ]
 
 FLAG_INDEX, FLAG_SLOT, FLAG_REQUEST, FLAG_COUNT, FLAG_TIMEOUT, FLAG_TOPK = 1, 2, 4, 8, 16, 32
 # values of PillarShape.schedule (PILLAR_SCHEDULE_* in the header)
-SCHEDULE_UNIFIED, SCHEDULE_DRAFT_ONLY, SCHEDULE_VERIFY_ONLY, SCHEDULE_UNIFORM_ROWS = 0, 1, 2, 3
+SCHEDULE_UNIFIED, SCHEDULE_DRAFT_ONLY, SCHEDULE_VERIFY_ONLY, SCHEDULE_UNIFORM_ROWS, SCHEDULE_NAIVE_JOINT = 0, 1, 2, 3, 4
 EXPORTED = ("pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_attn_unified_slotted",
             "pillar_draft_lists", "pillar_topk_workspace_bytes",
             "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string",

@@ -60,7 +60,7 @@ int check_shape(const pillar_shape_t *s) {
     // the pools are addressed as num_slots * Hkv rows with 32-bit row coordinates
     if (s->Hkv > 0 && s->num_slots > 0x7fffffffll / s->Hkv) return PILLAR_ERR_ARG;
     if (s->row_lo < 0 || s->row_hi > s->k + 1 || s->row_lo >= s->row_hi) return PILLAR_ERR_ARG;
-    if (s->schedule < PILLAR_SCHEDULE_UNIFIED || s->schedule > PILLAR_SCHEDULE_UNIFORM_ROWS) return PILLAR_ERR_ARG;
+    if (s->schedule < PILLAR_SCHEDULE_UNIFIED || s->schedule > PILLAR_SCHEDULE_NAIVE_JOINT) return PILLAR_ERR_ARG;
     if (s->wait_timeout_us < 0) return PILLAR_ERR_ARG;
     if (!(s->sm_scale >= 0.f) || std::isinf(s->sm_scale)) return PILLAR_ERR_ARG;
     for (int c : {s->verify_chunk, s->draft_chunk})
@@ -157,8 +157,9 @@ int pillar_attn_unified_slotted(const pillar_shape_t *shape, const uint16_t *q, 
     pa.k = s.k;
     pa.max_sparse = s.max_sparse;
     pa.max_len = s.max_len;
-    pa.vchunk = verify_chunk_of(s);
-    pa.dchunk = draft_chunk_of(s);
+    const bool naive = s.schedule == PILLAR_SCHEDULE_NAIVE_JOINT;  // the largest items the pipeline takes
+    pa.vchunk = naive ? kMaxChunk : verify_chunk_of(s);
+    pa.dchunk = naive ? kMaxChunk : draft_chunk_of(s);
     pa.schedule = s.schedule;
     if (launch_plan(pa, cs) != cudaSuccess) return PILLAR_ERR_CUDA;
 

@@ -80,6 +80,7 @@ struct AttnParams {
     long long num_slots;
     int Hq, Hkv, G, k, M, max_sparse;
     int RQ, RQd;  // query rows per TMEM lane quadrant: verify ceil(M / 4), draft ceil(G / 4)
+    int static_units;  // 1: the naive joint batch (CTA c takes units c, c + grid, ...; no queue)
     float scale;
     unsigned long long wait_ns;  // bound of every pipeline wait (the drains keep kWaitTimeoutNs)
 };
@@ -228,14 +229,32 @@ __device__ __forceinline__ int row_slot(int r, int RQ) {
 
 // ============================================================== resolver warp
 
+// The next item of a CTA under the naive joint batch: the items of units
+// blockIdx.x, blockIdx.x + gridDim.x, ... in order (unit cursor u, split s);
+// num_items when none is left.  A verify unit's items are listed head-minor
+// by the planner: split s of unit (b, g) is item item_base - g*ns + g + s*Hkv.
+__device__ __forceinline__ int static_next_item(const AttnParams &p, int num_items, int &u, int &s) {
+    const int U = *reinterpret_cast<volatile int *>(&p.hdr->num_units);
+    for (; u < U; u += gridDim.x, s = 0) {
+        const UnitInfo ui = p.unit[u];
+        if (s >= ui.nsplit) continue;
+        const int b = u / p.Hkv, g = u - b * p.Hkv;
+        const int it = p.req[b].mode == 1 ? ui.item_base - g * ui.nsplit + g + s * p.Hkv : ui.item_base + s;
+        ++s;
+        return it;
+    }
+    return num_items;
+}
+
 __device__ void resolver(const AttnParams &p, const Ctx &c, int lane) {
     const int num_items = *reinterpret_cast<volatile int *>(&p.hdr->num_items);
     uint32_t eph = 0;
+    int su = blockIdx.x, ss = 0;  // the naive joint batch's cursor
     for (int rb = 0;; rb = rb + 1 == kRowLists ? 0 : rb + 1) {
         if (!mbar_wait(&c.rempty[rb], ((eph >> rb) & 1) ^ 1, c.abort, c.err, c.wait_ns)) return;
         eph ^= 1u << rb;
         int it = 0;
-        if (lane == 0) it = atomicAdd(&p.hdr->item_counter, 1);
+        if (lane == 0) it = p.static_units ? static_next_item(p, num_items, su, ss) : atomicAdd(&p.hdr->item_counter, 1);
         it = __shfl_sync(0xffffffffu, it, 0);
         if (it >= num_items) {
             if (lane == 0) c.iinfo[rb].it = -1;
@@ -1207,8 +1226,10 @@ cudaError_t launch_attn(const AttnArgs &a, int nsm, cudaStream_t st) {
     p.M = (a.k + 1) * p.G;
     p.RQ = (p.M + kConsumerWarps - 1) / kConsumerWarps;
     // draft items spread their G rows over the four quadrants, except in the
-    // uniform-rows schedule, where they take the verify row layout
-    p.RQd = a.schedule == PILLAR_SCHEDULE_UNIFORM_ROWS ? p.RQ : (p.G + kConsumerWarps - 1) / kConsumerWarps;
+    // uniform-rows schedule and the naive joint batch, where they take the verify row layout
+    const bool naive = a.schedule == PILLAR_SCHEDULE_NAIVE_JOINT;
+    p.RQd = (a.schedule == PILLAR_SCHEDULE_UNIFORM_ROWS || naive) ? p.RQ : (p.G + kConsumerWarps - 1) / kConsumerWarps;
+    p.static_units = naive ? 1 : 0;
     p.max_sparse = a.max_sparse;
     p.scale = a.scale;
     p.wait_ns = a.wait_ns;

@@ -54,11 +54,11 @@ def _shape(**kw):
 def test_workspace_sizes_and_argument_checks(lib):
     n = P.pillar_attn_workspace_bytes(_shape())
     assert n > 0 and n % 256 == 0
-    for sched in (P.SCHEDULE_DRAFT_ONLY, P.SCHEDULE_VERIFY_ONLY, P.SCHEDULE_UNIFORM_ROWS):
+    for sched in (P.SCHEDULE_DRAFT_ONLY, P.SCHEDULE_VERIFY_ONLY, P.SCHEDULE_UNIFORM_ROWS, P.SCHEDULE_NAIVE_JOINT):
         assert P.pillar_attn_workspace_bytes(_shape(schedule=sched)) == n  # the schedule needs no other room
     assert P.pillar_topk_workspace_bytes(_shape(), 3) >= 3 * 8 * 8192 * 4
     for bad in (dict(D=96), dict(Hq=30), dict(k=15, Hq=40, Hkv=8), dict(max_len=0), dict(row_lo=3, row_hi=2),
-                dict(verify_chunk=100), dict(draft_chunk=8192), dict(Hq=72, Hkv=8), dict(schedule=4), dict(wait_timeout_us=-1),
+                dict(verify_chunk=100), dict(draft_chunk=8192), dict(Hq=72, Hkv=8), dict(schedule=5), dict(wait_timeout_us=-1),
                 dict(schedule=-1)):
         with pytest.raises(P.PillarError) as e:
             P.pillar_attn_workspace_bytes(_shape(**bad))

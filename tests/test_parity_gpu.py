@@ -107,7 +107,8 @@ def test_schedules_write_the_unified_outputs():
     """The sequential two-launch schedule (the draft requests, then the verify
     requests) writes exactly the values of one unified pass, each launch
     leaving the other mode's outputs untouched; the uniform-rows schedule
-    (draft items in the verify row layout) matches the oracle."""
+    (draft items in the verify row layout) and the naive joint batch match the
+    oracle."""
     import sparse_self_speculative_pillar_gb300 as P
     w = W.generate(W.scaled("qwen3_8b", B=19, length_scale=0.05, seed_offset=6))
     uni = Gpu(w, verify_chunk=128, draft_chunk=64)  # split units too
@@ -141,6 +142,25 @@ def test_schedules_write_the_unified_outputs():
     u.attn()
     assert u.attn_flags() == 0
     _check(w, u)
+
+    # the naive joint batch: largest items, the verify row layout, one CTA per unit in turn
+    n = Gpu(w, verify_chunk=128, draft_chunk=64, schedule=P.SCHEDULE_NAIVE_JOINT)
+    n.attn()
+    assert n.attn_flags() == 0
+    _check(w, n)
+
+
+def test_naive_joint_batch_on_long_contexts():
+    """The naive joint batch over contexts longer than one 2048-key item: a
+    CTA works through all items of its units (the split units' pieces are
+    merged as in the unified pass); the outputs match the oracle."""
+    import sparse_self_speculative_pillar_gb300 as P
+    w = W.generate(W.scaled("qwen3_8b", B=12, length_scale=0.6, seed_offset=8))
+    assert int(w.req_len[w.req_mode == 1].max()) > 2048
+    n = Gpu(w, schedule=P.SCHEDULE_NAIVE_JOINT)
+    n.attn()
+    assert n.attn_flags() == 0
+    _check(w, n)
 
 
 def test_repeated_calls_are_identical():
