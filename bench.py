@@ -355,6 +355,41 @@ def kv_append_timing(g, w, P, stream, n):
             "calls": n, "flags": int(dflag.item())}
 
 
+def kv_offload_timing(g, w, P, stream, n, n_req=4):
+    """The dynamic KV manager's copies ("SparseSpec-MLSys26", 动态 KV 管理):
+    the whole KV of the first n_req requests packed into page-locked host
+    memory by pillar_kv_offload and put back into the same slots by
+    pillar_kv_reload (so the pool is unchanged), each timed over n calls; the
+    host side is written and read by the kernels themselves (NVLink-C2C on a
+    Grace-Blackwell node)."""
+    import torch
+    from workloads.device import to_device
+    kvo = w.kv_off
+    idx = np.concatenate([np.arange(int(kvo[b]), int(kvo[b]) + int(w.req_len[b])) for b in range(min(n_req, w.B))])
+    slots = to_device(w.slot_table[idx].astype(np.int32))
+    hk = torch.empty((len(idx), w.Hkv, w.D), dtype=torch.int16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    dflag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    res = {"tokens": int(len(idx)), "bytes_each_way": int(len(idx) * w.Hkv * w.D * 2 * 2), "calls": n}
+    for name, call in (("offload", lambda: P.pillar_kv_offload(g.shape, g.k_pool, g.v_pool, slots, hk, hv, dflag,
+                                                                stream=stream)),
+                       ("reload", lambda: P.pillar_kv_reload(g.shape, hk, hv, slots, g.k_pool, g.v_pool, dflag,
+                                                              stream=stream))):
+        for _ in range(3):
+            call()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / n
+        res[name + "_us"] = us
+        res[name + "_gbs"] = res["bytes_each_way"] / (us * 1e-6) / 1e9
+    res["flags"] = int(dflag.item())
+    return res
+
+
 def draft_slots_timing(g, w, P, stream, n):
     """The draft lists with their pool slots already translated (as
     pillar_draft_lists writes them after a verify step's Top-K): the attention
@@ -583,6 +618,7 @@ def run_gpu(args):
     flags = g.attn_flags() | g.topk_flags()
     ablation = fusion_ablation(g, P, stream, max(10, min(args.steps, 500)))
     append = kv_append_timing(g, w, P, stream, max(10, min(args.steps, 500)))
+    offload = kv_offload_timing(g, w, P, stream, max(10, min(args.steps, 100)))
     slots = draft_slots_timing(g, w, P, stream, max(10, min(args.steps, 500)))
 
     if rank != 0:
@@ -628,6 +664,7 @@ def run_gpu(args):
                 "serial_value": serial_us},
         "fusion_ablation": ablation,
         "kv_append": append,
+        "kv_offload": offload,
         "draft_slots": slots,
         "layers": {"pools": n_layers, "bytes_per_layer": layer_bytes,
                    "rotation": "step i reads layer i mod pools: its own K/V pools (the same rows at other "

@@ -398,6 +398,115 @@ PILLAR_API int pillar_buckets_retire(pillar_buckets_t *pb, int32_t bucket);
 PILLAR_API int pillar_buckets_step(const pillar_buckets_t *pb, const int32_t *bucket, int32_t n, int64_t step,
                                    int32_t *req_mode, int32_t *phase, int64_t *q_rows);
 
+/*
+ * Host offload of KV ("SparseSpec-MLSys26", 动态 KV 管理 / the dynamic KV
+ * manager: when device memory runs short, requests' KV goes to host memory
+ * chunk by chunk, asynchronously, first in first out; requests that were
+ * offloaded are scheduled again, ahead of new ones, as soon as device memory
+ * is free).  Two parts: the copies of slot blocks between the page-size-1
+ * pools and packed rows in host memory (device kernels), and the FIFO of
+ * offloaded chunks (plain host code, caller-owned state).
+ */
+
+/*
+ * pillar_kv_offload -- packs n slot blocks of the pools into rows of host
+ * memory:
+ *   host_k[i, h, :] = k_pool[slots[i], h, :],  host_v[i, h, :] = v_pool[slots[i], h, :]
+ * for i < n and h < Hkv.  Only shape->Hkv, D and num_slots are used.
+ *   k_pool, v_pool [num_slots, Hkv, D] bf16, device memory, 16-byte aligned
+ *   slots          [n] int32, device memory (the slots of a request's chunk of
+ *                  positions, in position order)
+ *   host_k, host_v [n, Hkv, D] bf16, 16-byte aligned, page-locked host memory
+ *                  (cudaHostAlloc / cudaMallocHost / cudaHostRegister; the
+ *                  kernel writes it through its device mapping, over
+ *                  NVLink-C2C on a Grace-Blackwell node) or device memory
+ *   device_flags   device int32 or null: PILLAR_FLAG_SLOT is or-ed into it
+ *                  for a slot outside [0, num_slots); that row is not written
+ * Asynchronous on `stream` (the host rows are complete once the stream has
+ * reached the call); allocates nothing.  Returns PILLAR_OK, PILLAR_ERR_ARG
+ * (bad shape, n < 0, a null or misaligned pointer, or a host buffer the
+ * device cannot address: pageable host memory is refused) or PILLAR_ERR_CUDA.
+ */
+PILLAR_API int pillar_kv_offload(const pillar_shape_t *shape, const uint16_t *k_pool, const uint16_t *v_pool,
+                                 const int32_t *slots, int32_t n, uint16_t *host_k, uint16_t *host_v,
+                                 int32_t *device_flags, void *stream);
+
+/*
+ * pillar_kv_reload -- the way back: the packed rows go to (new) slots,
+ *   k_pool[slots[i], h, :] = host_k[i, h, :],  v_pool[slots[i], h, :] = host_v[i, h, :]
+ * with the buffers, alignment, flags and status codes of pillar_kv_offload
+ * (host_k and host_v are read, the pools written).  It is pillar_kv_append
+ * with its new rows in host memory.
+ */
+PILLAR_API int pillar_kv_reload(const pillar_shape_t *shape, const uint16_t *host_k, const uint16_t *host_v,
+                                const int32_t *slots, int32_t n, uint16_t *k_pool, uint16_t *v_pool,
+                                int32_t *device_flags, void *stream);
+
+/*
+ * The FIFO of offloaded chunks.  The state counts the device slots held by
+ * resident requests against a capacity, and queues the chunks of offloaded
+ * requests (a request's positions [0, len) in chunks of `chunk` positions,
+ * the last one possibly shorter) in the order they were offloaded.  A
+ * request comes back whole: pillar_offload_reload pops the chunks of the
+ * oldest offloaded requests while they fit in the free capacity, so a request
+ * offloaded earlier is always reloaded earlier, and a request never runs
+ * with part of its KV on the host.  Which request to offload is the caller's
+ * choice (the pages leave it open).  Every function returns PILLAR_OK or
+ * PILLAR_ERR_ARG (a null pointer or out-of-range argument) and changes
+ * nothing on error.  Nothing is allocated and no GPU is touched.
+ */
+#define PILLAR_OFFLOAD_QUEUE 1024
+typedef struct pillar_offload_chunk {
+    int32_t req;    /* the caller's request id */
+    int32_t first;  /* first position of the chunk */
+    int32_t n;      /* positions in the chunk (chunk, or fewer for the request's last) */
+    int32_t last;   /* 1 on the request's last chunk */
+} pillar_offload_chunk_t;
+typedef struct pillar_offload_fifo {
+    int64_t capacity;  /* device slots available to requests' KV */
+    int64_t resident;  /* slots held by resident requests */
+    int32_t chunk;     /* positions per chunk (>= 1) */
+    int32_t head;      /* queue index of the oldest chunk */
+    int32_t count;     /* chunks queued */
+    int32_t pad;
+    pillar_offload_chunk_t q[PILLAR_OFFLOAD_QUEUE];
+} pillar_offload_fifo_t;
+
+/* pillar_offload_init -- no request resident, nothing queued. */
+PILLAR_API int pillar_offload_init(pillar_offload_fifo_t *f, int64_t capacity, int32_t chunk);
+
+/*
+ * pillar_offload_reserve -- asks for n more device slots (a new request's KV,
+ * or the tokens a running request appends).  *granted = 1 and the slots are
+ * counted as resident if they fit; *granted = 0 otherwise, and also, for a
+ * new request (new_request != 0), while offloaded requests wait: they are
+ * brought back first.
+ */
+PILLAR_API int pillar_offload_reserve(pillar_offload_fifo_t *f, int64_t n, int32_t new_request, int32_t *granted);
+
+/* pillar_offload_release -- a resident request finished: its n slots are free. */
+PILLAR_API int pillar_offload_release(pillar_offload_fifo_t *f, int64_t n);
+
+/*
+ * pillar_offload_evict -- request `req` with len resident positions goes to
+ * the host: its chunks join the queue (*nchunks of them, nullable) and its
+ * slots stop counting as resident.  The caller copies each chunk's slot blocks
+ * with pillar_kv_offload before it hands those slots out again.  Refused
+ * (PILLAR_ERR_ARG) when the queue has no room for the chunks or len exceeds
+ * the resident count.
+ */
+PILLAR_API int pillar_offload_evict(pillar_offload_fifo_t *f, int32_t req, int32_t len, int32_t *nchunks);
+
+/*
+ * pillar_offload_reload -- the chunks to bring back now: those of the oldest
+ * offloaded requests, whole requests only, while their positions fit in the
+ * free capacity and their chunks in out[0, max_out).  They leave the queue and
+ * count as resident; *nout gets the number of chunks written (0: nothing fits
+ * yet).  The caller allocates slots for them and copies with pillar_kv_reload.
+ */
+PILLAR_API int pillar_offload_reload(pillar_offload_fifo_t *f, pillar_offload_chunk_t *out, int32_t max_out,
+                                     int32_t *nout);
+
 #ifdef __cplusplus
 }
 #endif

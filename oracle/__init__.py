@@ -178,6 +178,25 @@ def kv_append(k_pool, v_pool, k_new, v_new, slots):
     return k, v, skipped
 
 
+def kv_offload(k_pool, v_pool, slots):
+    """The packed rows an offload writes to host memory ("SparseSpec-MLSys26",
+    动态 KV 管理: a request's KV goes to the host chunk by chunk): row i holds
+    the slot block k_pool[slots[i]] / v_pool[slots[i]]; a slot outside
+    [0, num_slots) leaves its row as it was (zeros here) and is reported.
+    Returns (k_rows, v_rows, any_skipped).  One row at a time, in order."""
+    slots = np.asarray(slots).tolist()
+    k = np.zeros((len(slots),) + tuple(k_pool.shape[1:]), dtype=np.asarray(k_pool).dtype)
+    v = np.zeros((len(slots),) + tuple(v_pool.shape[1:]), dtype=np.asarray(v_pool).dtype)
+    skipped = False
+    for i, s in enumerate(slots):
+        if 0 <= s < k_pool.shape[0]:
+            k[i] = k_pool[s]
+            v[i] = v_pool[s]
+        else:
+            skipped = True
+    return k, v, skipped
+
+
 def draft_lists_after_topk(next_idx, next_cnt, verify_len, phase, slot_table=None, kv_off=None):
     """Critical lists of the draft steps that follow a verify step
     ("SparseSpec-MLSys26", PillarAttn: the Top-K of the verify step's exact

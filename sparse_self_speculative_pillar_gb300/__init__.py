@@ -16,9 +16,18 @@ Entry points (same names as the C ABI):
                      next_idx, next_cnt, workspace, stream=None)
   pillar_get_error(workspace, stream=None)
   pillar_status_string(status)
+  pillar_attn_unified_slotted(shape, ..., sparse_slot, out, ...)   (draft lists with their slots)
+  pillar_draft_lists(shape, V, next_idx, next_cnt, group_map, verify_len, req_len, slot_table,
+                     sparse_idx, sparse_cnt, sparse_slot=None, device_flags=None, stream=None)
+  pillar_topk_select_noalloc(shape, V, ..., device_flags=None, stream=None)
   pillar_kv_append(shape, k_new, v_new, slots, k_pool, v_pool, device_flags=None, stream=None)
+  pillar_kv_offload(shape, k_pool, v_pool, slots, host_k, host_v, device_flags=None, stream=None)
+  pillar_kv_reload(shape, host_k, host_v, slots, k_pool, v_pool, device_flags=None, stream=None)
   pillar_buckets_init(k), pillar_buckets_admit(pb), pillar_buckets_retire(pb, bucket),
   pillar_buckets_step(pb, buckets, step)    (host-side phase buckets)
+  pillar_offload_init(capacity, chunk), pillar_offload_reserve(f, n, new_request),
+  pillar_offload_release(f, n), pillar_offload_evict(f, req, len),
+  pillar_offload_reload(f, max_out)         (host-side FIFO of offloaded KV chunks)
 """
 from __future__ import annotations
 
@@ -34,6 +43,8 @@ __all__ = [
     "FLAG_INDEX", "FLAG_SLOT", "FLAG_REQUEST", "FLAG_COUNT", "FLAG_TIMEOUT", "FLAG_TOPK",
     "SCHEDULE_UNIFIED", "SCHEDULE_DRAFT_ONLY", "SCHEDULE_VERIFY_ONLY", "SCHEDULE_UNIFORM_ROWS", "SCHEDULE_NAIVE_JOINT",
     "pillar_kv_append", "PillarBuckets", "pillar_buckets_init", "pillar_buckets_admit", "pillar_buckets_retire", "pillar_buckets_step",
+    "pillar_kv_offload", "pillar_kv_reload", "PillarOffloadFifo", "pillar_offload_init", "pillar_offload_reserve",
+    "pillar_offload_release", "pillar_offload_evict", "pillar_offload_reload",
 ]
 
 FLAG_INDEX, FLAG_SLOT, FLAG_REQUEST, FLAG_COUNT, FLAG_TIMEOUT, FLAG_TOPK = 1, 2, 4, 8, 16, 32
@@ -43,8 +54,10 @@ EXPORTED = ("pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_attn_u
             "pillar_draft_lists", "pillar_topk_workspace_bytes",
             "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string",
             "pillar_kv_append", "pillar_buckets_init", "pillar_buckets_admit", "pillar_buckets_retire",
-            "pillar_buckets_step")
+            "pillar_buckets_step", "pillar_kv_offload", "pillar_kv_reload", "pillar_offload_init",
+            "pillar_offload_reserve", "pillar_offload_release", "pillar_offload_evict", "pillar_offload_reload")
 MAX_BUCKETS = 64  # PILLAR_MAX_BUCKETS
+OFFLOAD_QUEUE = 1024  # PILLAR_OFFLOAD_QUEUE
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024 + 256
 
 
@@ -66,6 +79,18 @@ def make_shape(*, B, Hq, Hkv, D, k, max_sparse, max_len, num_slots, max_topk=1, 
                        row_lo=row_lo, row_hi=(k + 1) if row_hi is None else row_hi, max_topk=max(1, max_topk),
                        verify_chunk=verify_chunk, draft_chunk=draft_chunk, num_slots=num_slots,
                        sm_scale=sm_scale, schedule=schedule, wait_timeout_us=wait_timeout_us)
+
+
+class PillarOffloadChunk(ctypes.Structure):
+    """pillar_offload_chunk_t: one chunk of an offloaded request's positions."""
+    _fields_ = [("req", ctypes.c_int32), ("first", ctypes.c_int32), ("n", ctypes.c_int32), ("last", ctypes.c_int32)]
+
+
+class PillarOffloadFifo(ctypes.Structure):
+    """pillar_offload_fifo_t: resident slot count and the queue of offloaded chunks."""
+    _fields_ = [("capacity", ctypes.c_int64), ("resident", ctypes.c_int64), ("chunk", ctypes.c_int32),
+                ("head", ctypes.c_int32), ("count", ctypes.c_int32), ("pad", ctypes.c_int32),
+                ("q", PillarOffloadChunk * OFFLOAD_QUEUE)]
 
 
 class PillarBuckets(ctypes.Structure):
@@ -123,6 +148,14 @@ def load():
     lib.pillar_buckets_retire.argtypes = [BP, ctypes.c_int32]
     lib.pillar_buckets_step.argtypes = [BP, I32P, ctypes.c_int32, ctypes.c_int64, I32P, I32P,
                                         ctypes.POINTER(ctypes.c_int64)]
+    lib.pillar_kv_offload.argtypes = [SP, P, P, P, ctypes.c_int32, P, P, P, P]
+    lib.pillar_kv_reload.argtypes = [SP, P, P, P, ctypes.c_int32, P, P, P, P]
+    FP = ctypes.POINTER(PillarOffloadFifo)
+    lib.pillar_offload_init.argtypes = [FP, ctypes.c_int64, ctypes.c_int32]
+    lib.pillar_offload_reserve.argtypes = [FP, ctypes.c_int64, ctypes.c_int32, I32P]
+    lib.pillar_offload_release.argtypes = [FP, ctypes.c_int64]
+    lib.pillar_offload_evict.argtypes = [FP, ctypes.c_int32, ctypes.c_int32, I32P]
+    lib.pillar_offload_reload.argtypes = [FP, ctypes.POINTER(PillarOffloadChunk), ctypes.c_int32, I32P]
     lib.pillar_status_string.restype = ctypes.c_char_p
     for n in EXPORTED:
         if n == "pillar_status_string":
@@ -258,6 +291,79 @@ def pillar_kv_append(shape, k_new, v_new, slots, k_pool, v_pool, device_flags=No
                                  _ptr(v_pool), _ptr(device_flags), _stream(stream))
     if st:
         raise PillarError("pillar_kv_append", st)
+
+
+def _host_ptr(x):
+    """Address of a host buffer for the offload copies (a CPU tensor, page-locked
+    or not: the library refuses memory the device cannot address), a CUDA
+    tensor, or a raw int pointer."""
+    if x is None or isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def pillar_kv_offload(shape, k_pool, v_pool, slots, host_k, host_v, device_flags=None, stream=None):
+    """Pack the slot blocks k_pool[slots[i]], v_pool[slots[i]] into rows i of
+    host_k, host_v ([n, Hkv, D] bf16, page-locked host memory, e.g. a tensor
+    made with pin_memory=True); out-of-range slots are skipped and flagged."""
+    n = int(slots.numel())
+    st = load().pillar_kv_offload(ctypes.byref(shape), _ptr(k_pool), _ptr(v_pool), _ptr(slots), n,
+                                  _host_ptr(host_k), _host_ptr(host_v), _ptr(device_flags), _stream(stream))
+    if st:
+        raise PillarError("pillar_kv_offload", st)
+
+
+def pillar_kv_reload(shape, host_k, host_v, slots, k_pool, v_pool, device_flags=None, stream=None):
+    """The way back: rows i of host_k, host_v go to the slot blocks slots[i]."""
+    n = int(slots.numel())
+    st = load().pillar_kv_reload(ctypes.byref(shape), _host_ptr(host_k), _host_ptr(host_v), _ptr(slots), n,
+                                 _ptr(k_pool), _ptr(v_pool), _ptr(device_flags), _stream(stream))
+    if st:
+        raise PillarError("pillar_kv_reload", st)
+
+
+# --------------------------------------------------------------- offload FIFO (host side)
+
+def pillar_offload_init(capacity: int, chunk: int) -> PillarOffloadFifo:
+    f = PillarOffloadFifo()
+    st = load().pillar_offload_init(ctypes.byref(f), int(capacity), int(chunk))
+    if st:
+        raise PillarError("pillar_offload_init", st)
+    return f
+
+
+def pillar_offload_reserve(f: PillarOffloadFifo, n: int, new_request: bool) -> bool:
+    """True if n more device slots were granted (see the header)."""
+    g = ctypes.c_int32(0)
+    st = load().pillar_offload_reserve(ctypes.byref(f), int(n), 1 if new_request else 0, ctypes.byref(g))
+    if st:
+        raise PillarError("pillar_offload_reserve", st)
+    return bool(g.value)
+
+
+def pillar_offload_release(f: PillarOffloadFifo, n: int) -> None:
+    st = load().pillar_offload_release(ctypes.byref(f), int(n))
+    if st:
+        raise PillarError("pillar_offload_release", st)
+
+
+def pillar_offload_evict(f: PillarOffloadFifo, req: int, length: int) -> int:
+    """Queue request `req`'s positions [0, length) for the host; returns its chunk count."""
+    nc = ctypes.c_int32(0)
+    st = load().pillar_offload_evict(ctypes.byref(f), int(req), int(length), ctypes.byref(nc))
+    if st:
+        raise PillarError("pillar_offload_evict", st)
+    return int(nc.value)
+
+
+def pillar_offload_reload(f: PillarOffloadFifo, max_out: int = OFFLOAD_QUEUE):
+    """Chunks to bring back now, as (req, first, n, last) tuples, oldest requests first."""
+    out = (PillarOffloadChunk * max(1, max_out))()
+    nout = ctypes.c_int32(0)
+    st = load().pillar_offload_reload(ctypes.byref(f), out, int(max_out), ctypes.byref(nout))
+    if st:
+        raise PillarError("pillar_offload_reload", st)
+    return [(c.req, c.first, c.n, c.last) for c in out[:nout.value]]
 
 
 # --------------------------------------------------------------- phase buckets (host side)

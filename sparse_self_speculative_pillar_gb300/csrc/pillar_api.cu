@@ -270,6 +270,68 @@ int pillar_kv_append(const pillar_shape_t *shape, const uint16_t *k_new, const u
     return launch_kv_append(a, nsm, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PILLAR_OK : PILLAR_ERR_CUDA;
 }
 
+// The device address of a buffer the offload copies read or write: device
+// memory as it is, page-locked host memory through its mapping; anything else
+// (pageable host memory) is refused rather than handed to a kernel.
+static void *device_address(void *p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // (the failed query leaves an error that the next check would see)
+        return nullptr;
+    }
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return p;
+    if (at.type == cudaMemoryTypeHost) return at.devicePointer;
+    return nullptr;
+}
+
+static int kv_copy_checks(const pillar_shape_t *shape, int32_t n, const void *a, const void *b, const void *c,
+                          const void *d, const int32_t *slots, const int32_t *device_flags) {
+    const int st = check_shape(shape);
+    if (st != PILLAR_OK) return st;
+    if (n < 0) return PILLAR_ERR_ARG;
+    if (n == 0) return PILLAR_OK;
+    if (!a || !b || !c || !d || !slots) return PILLAR_ERR_ARG;
+    if (!aligned(a, 16) || !aligned(b, 16) || !aligned(c, 16) || !aligned(d, 16) || !aligned(slots, 4) ||
+        (device_flags && !aligned(device_flags, 4)))
+        return PILLAR_ERR_ARG;
+    return PILLAR_OK;
+}
+
+int pillar_kv_offload(const pillar_shape_t *shape, const uint16_t *k_pool, const uint16_t *v_pool,
+                      const int32_t *slots, int32_t n, uint16_t *host_k, uint16_t *host_v, int32_t *device_flags,
+                      void *stream) {
+    const int st = kv_copy_checks(shape, n, k_pool, v_pool, host_k, host_v, slots, device_flags);
+    if (st != PILLAR_OK || n == 0) return st;
+    void *ko = device_address(host_k), *vo = device_address(host_v);
+    if (!ko || !vo) return PILLAR_ERR_ARG;
+    const int nsm = sm_count();
+    if (nsm <= 0) return PILLAR_ERR_CUDA;
+    KvOffloadArgs a;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.slots = slots;
+    a.k_out = static_cast<uint16_t *>(ko);
+    a.v_out = static_cast<uint16_t *>(vo);
+    a.flags = device_flags;
+    a.num_slots = shape->num_slots;
+    a.n = n;
+    a.Hkv = shape->Hkv;
+    a.D = shape->D;
+    return launch_kv_offload(a, nsm, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PILLAR_OK : PILLAR_ERR_CUDA;
+}
+
+int pillar_kv_reload(const pillar_shape_t *shape, const uint16_t *host_k, const uint16_t *host_v,
+                     const int32_t *slots, int32_t n, uint16_t *k_pool, uint16_t *v_pool, int32_t *device_flags,
+                     void *stream) {
+    const int st = kv_copy_checks(shape, n, host_k, host_v, k_pool, v_pool, slots, device_flags);
+    if (st != PILLAR_OK || n == 0) return st;
+    void *ki = device_address(const_cast<uint16_t *>(host_k)), *vi = device_address(const_cast<uint16_t *>(host_v));
+    if (!ki || !vi) return PILLAR_ERR_ARG;
+    // the reload is the append's scatter, its packed rows read through their device address
+    return pillar_kv_append(shape, static_cast<const uint16_t *>(ki), static_cast<const uint16_t *>(vi), slots, n,
+                            k_pool, v_pool, device_flags, stream);
+}
+
 int pillar_draft_lists(const pillar_shape_t *shape, int32_t V, const int32_t *next_idx, const int32_t *next_cnt,
                        const int32_t *group_map, const int32_t *verify_len, const int32_t *req_len,
                        const int32_t *slot_table, int32_t *sparse_idx, int32_t *sparse_cnt, int32_t *sparse_slot,

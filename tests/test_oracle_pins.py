@@ -491,6 +491,30 @@ def test_kv_append_pins():
     assert not skipped and np.array_equal(k3, k) and np.array_equal(v3, v)
 
 
+def test_kv_offload_pins():
+    """The offload gathers the listed slot blocks in list order (a repeated
+    slot gives the same row twice), reports out-of-range slots with their
+    rows left zero, and appending its rows back to the same slots restores the
+    pools; appending them to other slots moves the request's KV there."""
+    rng = np.random.default_rng(4)
+    k = rng.integers(-9, 9, (10, 3, 4)).astype(np.int16)
+    v = rng.integers(-9, 9, (10, 3, 4)).astype(np.int16)
+    slots = np.array([7, 2, 2, 9, 0], np.int32)
+    ko, vo, skipped = oracle.kv_offload(k, v, slots)
+    assert not skipped and ko.shape == (5, 3, 4)
+    for i, s in enumerate(slots):
+        assert np.array_equal(ko[i], k[s]) and np.array_equal(vo[i], v[s])
+    k2, v2, _ = oracle.kv_append(np.zeros_like(k), np.zeros_like(v), ko, vo, slots)
+    for s in set(slots.tolist()):
+        assert np.array_equal(k2[s], k[s]) and np.array_equal(v2[s], v[s])
+    kb, vb, skipped = oracle.kv_offload(k, v, np.array([3, 10, -1], np.int32))
+    assert skipped and np.array_equal(kb[0], k[3]) and not kb[1:].any() and not vb[1:].any()
+    moved = np.array([1, 4, 5, 6, 8], np.int32)  # the same rows, new slots
+    k3, v3, _ = oracle.kv_append(k, v, ko, vo, moved)
+    for i, s in enumerate(moved):
+        assert np.array_equal(k3[s], k[slots[i]]) and np.array_equal(v3[s], v[slots[i]])
+
+
 def test_draft_lists_after_topk_rebuild_the_generator_lists():
     """The workload generator builds each draft request's list independently
     (a critical subset of [0, L-p) plus the p newest positions); feeding the
