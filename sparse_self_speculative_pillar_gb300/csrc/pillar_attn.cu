@@ -18,9 +18,10 @@
 // shared memory), sixteen warps per CTA in four groups (registers move to
 // the softmax group with setmaxnreg):
 //   * resolver warp: pops work items from a global atomic counter, reads the
-//     item's records and translates its positions into pool slots (list ->
-//     slot, many independent loads per lane) into a ring of three row lists,
-//     up to two items ahead of the loaders;
+//     item's records and translates its positions into pool slots (a verify
+//     item's slots are one run of the slot table, read 32 per lane in one
+//     round trip; a draft list is read 16 per lane, list -> slot) into a ring
+//     of three row lists, up to two items ahead of the loaders;
 //   * four loader warps: gather the item's K/V rows into the stage ring with
 //     TMA tile::gather4 (four 256-byte page-size-1 rows per copy) in the
 //     swizzled layout the tensor cores read, completion counted in bytes on
@@ -276,13 +277,37 @@ __device__ void resolver(const AttnParams &p, const Ctx &c, int lane) {
         const int *slist = (!verify && p.sparse_slot) ? p.sparse_slot + lrow : nullptr;
         int *rows = c.rowlist + rb * kMaxChunk;
         int bad = 0;
-        // 16 independent loads per lane keep the dependent list -> slot chain short
+        if (verify) {
+            // a verify item's slots are one contiguous run of the slot table: 32 independent
+            // loads per lane, one round trip for the 1024 keys of a default item
+            for (int base = 0; base < n; base += 32 * 32) {
+                int slot[32];
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    const int i = base + r * 32 + lane;
+                    slot[r] = i < n ? __ldg(p.slot_table + kvo + itm.begin + i) : -1;
+                }
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    const int i = base + r * 32 + lane;
+                    if (i < n) {
+                        int s = slot[r];
+                        if (s < 0 || (long long)s >= p.num_slots) {
+                            bad |= PILLAR_FLAG_SLOT;
+                            s = -1;
+                        }
+                        rows[i] = s;
+                    }
+                }
+            }
+        } else
+        // draft lists: 16 independent loads per lane keep the dependent list -> slot chain short
         for (int base = 0; base < n; base += 32 * 16) {
             int pos[16], slot[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 const int i = base + r * 32 + lane;
-                pos[r] = i < n ? (verify ? itm.begin + i : __ldg(list + i)) : -1;
+                pos[r] = i < n ? __ldg(list + i) : -1;
                 if (slist) slot[r] = i < n ? __ldg(slist + i) : -1;
             }
 #pragma unroll
