@@ -201,6 +201,38 @@ PILLAR_API int pillar_attn_unified_slotted(const pillar_shape_t *shape, const ui
                                            float *verify_lse, void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * pillar_attn_plan + pillar_attn_run -- pillar_attn_unified in two calls, so
+ * that one plan serves several runs.  The plan depends only on the batch
+ * description (req_mode, req_len, sparse_cnt), which is the same for every
+ * layer of a model step; the runs take what differs per layer (q, the pools,
+ * the lists, the outputs).  pillar_attn_unified(_slotted) is exactly a plan
+ * followed by a run.
+ *
+ * pillar_attn_plan(shape, req_mode, req_len, sparse_cnt, workspace, ...)
+ *   launches the device planner: it clears the workspace's error word and
+ *   writes the offsets, work items and partial-record layout into the
+ *   workspace.  Arguments as in pillar_attn_unified; with B == 0 it only
+ *   clears the error word.
+ * pillar_attn_run(shape, q, k_pool, v_pool, slot_table, sparse_idx,
+ *                 sparse_slot, out, verify_logits, verify_lse, workspace, ...)
+ *   launches the attention kernel and the merge of split units on the plan in
+ *   the workspace; sparse_slot may be NULL (as pillar_attn_unified_slotted).
+ *   The shape must be the one the plan was made with, the inputs must have the
+ *   plan's batch description (the same modes, lengths and list counts), and the
+ *   plan must precede the run on the stream (or be complete).  Any number of
+ *   runs may follow one plan, one after the other on a stream; the error word
+ *   collects the flags of the plan and of every run until pillar_get_error
+ *   reads and clears it.
+ * Return codes as pillar_attn_unified; a run with B == 0 does nothing.
+ */
+PILLAR_API int pillar_attn_plan(const pillar_shape_t *shape, const int32_t *req_mode, const int32_t *req_len,
+                                const int32_t *sparse_cnt, void *workspace, size_t ws_bytes, void *stream);
+PILLAR_API int pillar_attn_run(const pillar_shape_t *shape, const uint16_t *q, const uint16_t *k_pool,
+                               const uint16_t *v_pool, const int32_t *slot_table, const int32_t *sparse_idx,
+                               const int32_t *sparse_slot, uint16_t *out, float *verify_logits, float *verify_lse,
+                               void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * pillar_topk_workspace_bytes -- workspace of pillar_topk_select for V
  * verify requests of length <= max_len.  Returns PILLAR_OK or PILLAR_ERR_ARG
  * (a bad shape, V < 0, or V * Hkv * max_len fp32 scores past 2^50 bytes).

@@ -17,6 +17,9 @@ Entry points (same names as the C ABI):
   pillar_get_error(workspace, stream=None)
   pillar_status_string(status)
   pillar_attn_unified_slotted(shape, ..., sparse_slot, out, ...)   (draft lists with their slots)
+  pillar_attn_plan(shape, req_mode, req_len, sparse_cnt, workspace, stream=None)
+  pillar_attn_run(shape, q, k_pool, v_pool, slot_table, sparse_idx, out, verify_logits, verify_lse,
+                  workspace, sparse_slot=None, stream=None)  (one plan, several runs)
   pillar_draft_lists(shape, V, next_idx, next_cnt, group_map, verify_len, req_len, slot_table,
                      sparse_idx, sparse_cnt, sparse_slot=None, device_flags=None, stream=None)
   pillar_topk_select_noalloc(shape, V, ..., device_flags=None, stream=None)
@@ -39,6 +42,7 @@ from . import _build
 __all__ = [
     "PillarShape", "make_shape", "PillarError", "load", "library_path", "build",
     "pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_attn_unified_slotted", "pillar_draft_lists",
+    "pillar_attn_plan", "pillar_attn_run",
     "pillar_topk_workspace_bytes", "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string",
     "FLAG_INDEX", "FLAG_SLOT", "FLAG_REQUEST", "FLAG_COUNT", "FLAG_TIMEOUT", "FLAG_TOPK",
     "SCHEDULE_UNIFIED", "SCHEDULE_DRAFT_ONLY", "SCHEDULE_VERIFY_ONLY", "SCHEDULE_UNIFORM_ROWS", "SCHEDULE_NAIVE_JOINT",
@@ -55,6 +59,7 @@ EXPORTED = ("pillar_attn_workspace_bytes", "pillar_attn_unified", "pillar_attn_u
             "pillar_topk_select", "pillar_topk_select_noalloc", "pillar_get_error", "pillar_status_string",
             "pillar_kv_append", "pillar_buckets_init", "pillar_buckets_admit", "pillar_buckets_retire",
             "pillar_buckets_step", "pillar_kv_offload", "pillar_kv_reload", "pillar_offload_init",
+            "pillar_attn_plan", "pillar_attn_run",
             "pillar_offload_reserve", "pillar_offload_release", "pillar_offload_evict", "pillar_offload_reload")
 MAX_BUCKETS = 64  # PILLAR_MAX_BUCKETS
 OFFLOAD_QUEUE = 1024  # PILLAR_OFFLOAD_QUEUE
@@ -135,6 +140,8 @@ def load():
     lib.pillar_attn_unified.argtypes = [SP] + [P] * 11 + [P, ctypes.c_size_t, P]
     lib.pillar_attn_unified_slotted.argtypes = [SP] + [P] * 12 + [P, ctypes.c_size_t, P]
     lib.pillar_draft_lists.argtypes = [SP, ctypes.c_int32] + [P] * 11
+    lib.pillar_attn_plan.argtypes = [SP, P, P, P, P, ctypes.c_size_t, P]
+    lib.pillar_attn_run.argtypes = [SP] + [P] * 10 + [ctypes.c_size_t, P]
     lib.pillar_topk_workspace_bytes.argtypes = [SP, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]
     lib.pillar_topk_select.argtypes = [SP, ctypes.c_int32] + [P] * 7 + [P, ctypes.c_size_t, P]
     lib.pillar_topk_select_noalloc.argtypes = [SP, ctypes.c_int32] + [P] * 8 + [P]
@@ -228,6 +235,25 @@ def pillar_attn_unified_slotted(shape, q, k_pool, v_pool, slot_table, req_mode, 
         _ptr(workspace), ws_bytes if ws_bytes is not None else _nbytes(workspace), _stream(stream))
     if st:
         raise PillarError("pillar_attn_unified_slotted", st)
+
+
+def pillar_attn_plan(shape, req_mode, req_len, sparse_cnt, workspace, stream=None, ws_bytes=None):
+    """The device planner alone: offsets and work items of the batch, into the workspace."""
+    st = load().pillar_attn_plan(ctypes.byref(shape), _ptr(req_mode), _ptr(req_len), _ptr(sparse_cnt), _ptr(workspace),
+                                 ws_bytes if ws_bytes is not None else _nbytes(workspace), _stream(stream))
+    if st:
+        raise PillarError("pillar_attn_plan", st)
+
+
+def pillar_attn_run(shape, q, k_pool, v_pool, slot_table, sparse_idx, out, verify_logits, verify_lse, workspace,
+                    sparse_slot=None, stream=None, ws_bytes=None):
+    """The attention kernel and the merge on the plan in the workspace (one layer of the batch the plan describes)."""
+    st = load().pillar_attn_run(
+        ctypes.byref(shape), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(slot_table), _ptr(sparse_idx), _ptr(sparse_slot),
+        _ptr(out), _ptr(verify_logits), _ptr(verify_lse), _ptr(workspace),
+        ws_bytes if ws_bytes is not None else _nbytes(workspace), _stream(stream))
+    if st:
+        raise PillarError("pillar_attn_run", st)
 
 
 def pillar_draft_lists(shape, V, next_idx, next_cnt, group_map, verify_len, req_len, slot_table, sparse_idx,

@@ -100,6 +100,28 @@ int pillar_attn_workspace_bytes(const pillar_shape_t *shape, size_t *bytes) {
     return PILLAR_OK;
 }
 
+// The host checks of an attention run (everything but the planner's inputs).
+static int attn_run_checks(const pillar_shape_t *shape, const uint16_t *q, const uint16_t *k_pool,
+                           const uint16_t *v_pool, const int32_t *slot_table, const int32_t *sparse_idx,
+                           const int32_t *sparse_slot, const uint16_t *out, const float *verify_logits,
+                           const float *verify_lse, const void *workspace, size_t ws_bytes) {
+    const int st = check_shape(shape);
+    if (st != PILLAR_OK) return st;
+    const pillar_shape_t &s = *shape;
+    if (s.B == 0) return PILLAR_OK;
+    if (!q || !k_pool || !v_pool || !slot_table || !out || !verify_logits || !verify_lse) return PILLAR_ERR_ARG;
+    if (s.max_sparse > 0 && !sparse_idx) return PILLAR_ERR_ARG;
+    // TMA and 16-byte copies need 16-byte aligned rows; the logit dump stores pairs (8 bytes);
+    // everything else is read or written in 4-byte words
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 4) ||
+        !aligned(verify_logits, 8) || !aligned(verify_lse, 4) || !aligned(slot_table, 4) ||
+        (sparse_idx && !aligned(sparse_idx, 4)) || (sparse_slot && !aligned(sparse_slot, 4)))
+        return PILLAR_ERR_ARG;
+    if (sparse_slot && !sparse_idx) return PILLAR_ERR_ARG;
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < attn_layout(s).total) return PILLAR_ERR_WORKSPACE;
+    return PILLAR_OK;
+}
+
 int pillar_attn_unified(const pillar_shape_t *shape, const uint16_t *q, const uint16_t *k_pool,
                         const uint16_t *v_pool, const int32_t *slot_table, const int32_t *req_mode,
                         const int32_t *req_len, const int32_t *sparse_idx, const int32_t *sparse_cnt,
@@ -115,41 +137,37 @@ int pillar_attn_unified_slotted(const pillar_shape_t *shape, const uint16_t *q, 
                                 const int32_t *req_len, const int32_t *sparse_idx, const int32_t *sparse_cnt,
                                 const int32_t *sparse_slot, uint16_t *out, float *verify_logits,
                                 float *verify_lse, void *workspace, size_t ws_bytes, void *stream) {
+    // the run's checks first, so that a bad call enqueues nothing
+    const int st = attn_run_checks(shape, q, k_pool, v_pool, slot_table, sparse_idx, sparse_slot, out, verify_logits,
+                                   verify_lse, workspace, ws_bytes);
+    if (st != PILLAR_OK) return st;
+    const int sp = pillar_attn_plan(shape, req_mode, req_len, sparse_cnt, workspace, ws_bytes, stream);
+    if (sp != PILLAR_OK) return sp;
+    return pillar_attn_run(shape, q, k_pool, v_pool, slot_table, sparse_idx, sparse_slot, out, verify_logits,
+                           verify_lse, workspace, ws_bytes, stream);
+}
+
+int pillar_attn_plan(const pillar_shape_t *shape, const int32_t *req_mode, const int32_t *req_len,
+                     const int32_t *sparse_cnt, void *workspace, size_t ws_bytes, void *stream) {
     int st = check_shape(shape);
     if (st != PILLAR_OK) return st;
     const pillar_shape_t &s = *shape;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (s.B == 0) {
-        // nothing to compute; a workspace passed in still reads back as clean
-        if (workspace && ws_bytes >= sizeof(WsHeader) &&
-            cudaMemsetAsync(workspace, 0, sizeof(int), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        // nothing to plan; a workspace passed in still reads back as clean
+        if (workspace && ws_bytes >= sizeof(WsHeader) && cudaMemsetAsync(workspace, 0, sizeof(int), cs) != cudaSuccess)
             return PILLAR_ERR_CUDA;
         return PILLAR_OK;
     }
-    if (!q || !k_pool || !v_pool || !slot_table || !req_mode || !req_len || !sparse_cnt || !out ||
-        !verify_logits || !verify_lse)
-        return PILLAR_ERR_ARG;
-    if (s.max_sparse > 0 && !sparse_idx) return PILLAR_ERR_ARG;
-    // TMA and 16-byte copies need 16-byte aligned rows; the logit dump stores pairs (8 bytes);
-    // everything else is read or written in 4-byte words
-    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 4) ||
-        !aligned(verify_logits, 8) || !aligned(verify_lse, 4) || !aligned(slot_table, 4) || !aligned(req_mode, 4) ||
-        !aligned(req_len, 4) || !aligned(sparse_cnt, 4) || (sparse_idx && !aligned(sparse_idx, 4)) ||
-        (sparse_slot && !aligned(sparse_slot, 4)))
-        return PILLAR_ERR_ARG;
-    if (sparse_slot && !sparse_idx) return PILLAR_ERR_ARG;
+    if (!req_mode || !req_len || !sparse_cnt) return PILLAR_ERR_ARG;
+    if (!aligned(req_mode, 4) || !aligned(req_len, 4) || !aligned(sparse_cnt, 4)) return PILLAR_ERR_ARG;
     const AttnLayout lay = attn_layout(s);
     if (!workspace || !aligned(workspace, 256) || ws_bytes < lay.total) return PILLAR_ERR_WORKSPACE;
-    const int nsm = sm_count();
-    if (nsm <= 0) return PILLAR_ERR_CUDA;
-
-    char *ws = static_cast<char *>(workspace);
-    cudaStream_t cs = static_cast<cudaStream_t>(stream);
-
     PlanArgs pa;
     pa.req_mode = req_mode;
     pa.req_len = req_len;
     pa.sparse_cnt = sparse_cnt;
-    pa.ws = ws;
+    pa.ws = static_cast<char *>(workspace);
     pa.lay = lay;
     pa.B = s.B;
     pa.Hq = s.Hq;
@@ -161,8 +179,19 @@ int pillar_attn_unified_slotted(const pillar_shape_t *shape, const uint16_t *q, 
     pa.vchunk = naive ? kMaxChunk : verify_chunk_of(s);
     pa.dchunk = naive ? kMaxChunk : draft_chunk_of(s);
     pa.schedule = s.schedule;
-    if (launch_plan(pa, cs) != cudaSuccess) return PILLAR_ERR_CUDA;
+    return launch_plan(pa, cs) == cudaSuccess ? PILLAR_OK : PILLAR_ERR_CUDA;
+}
 
+int pillar_attn_run(const pillar_shape_t *shape, const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                    const int32_t *slot_table, const int32_t *sparse_idx, const int32_t *sparse_slot, uint16_t *out,
+                    float *verify_logits, float *verify_lse, void *workspace, size_t ws_bytes, void *stream) {
+    const int st = attn_run_checks(shape, q, k_pool, v_pool, slot_table, sparse_idx, sparse_slot, out, verify_logits,
+                                   verify_lse, workspace, ws_bytes);
+    if (st != PILLAR_OK) return st;
+    const pillar_shape_t &s = *shape;
+    if (s.B == 0) return PILLAR_OK;
+    const int nsm = sm_count();
+    if (nsm <= 0) return PILLAR_ERR_CUDA;
     AttnArgs aa;
     aa.q = q;
     aa.k_pool = k_pool;
@@ -173,8 +202,8 @@ int pillar_attn_unified_slotted(const pillar_shape_t *shape, const uint16_t *q, 
     aa.out = out;
     aa.logits = verify_logits;
     aa.lse = verify_lse;
-    aa.ws = ws;
-    aa.lay = lay;
+    aa.ws = static_cast<char *>(workspace);
+    aa.lay = attn_layout(s);
     aa.num_slots = s.num_slots;
     aa.Hq = s.Hq;
     aa.Hkv = s.Hkv;
@@ -184,8 +213,7 @@ int pillar_attn_unified_slotted(const pillar_shape_t *shape, const uint16_t *q, 
     aa.schedule = s.schedule;
     aa.scale = s.sm_scale > 0.f ? s.sm_scale : 1.0f / std::sqrt((float)s.D);
     aa.wait_ns = s.wait_timeout_us > 0 ? (unsigned long long)s.wait_timeout_us * 1000ull : kWaitTimeoutNs;
-    if (launch_attn(aa, nsm, cs) != cudaSuccess) return PILLAR_ERR_CUDA;
-    return PILLAR_OK;
+    return launch_attn(aa, nsm, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PILLAR_OK : PILLAR_ERR_CUDA;
 }
 
 int pillar_topk_workspace_bytes(const pillar_shape_t *shape, int32_t V, size_t *bytes) {

@@ -1083,6 +1083,8 @@ constexpr int kMergeCtasPerSm = 1;  // one large CTA per SM: the whole grid is r
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(const AttnParams p) {
     pdl_wait_prerequisites();  // the partials come from the attention kernel
+    // the attention kernel is complete: its work queue is reset for the next run on the same plan
+    if (blockIdx.x == 0 && threadIdx.x == 0) p.hdr->item_counter = 0;
     const int per_unit = p.M * (D / 4);  // thread slots per listed unit (rows up to M)
     for (long long w = (long long)blockIdx.x * kMergeThreads + threadIdx.x; w < (long long)p.merge_cap * per_unit;
          w += (long long)gridDim.x * kMergeThreads) {

@@ -163,6 +163,38 @@ def test_naive_joint_batch_on_long_contexts():
     _check(w, n)
 
 
+def test_one_plan_serves_several_runs():
+    """pillar_attn_plan once, then pillar_attn_run for two layers of the same
+    batch (the second with every key's sign flipped, exact in bf16): the first
+    run writes bit for bit what the unified call writes, the second matches the
+    oracle over the flipped keys, and split units are merged in both (small
+    item sizes)."""
+    import copy
+    import sparse_self_speculative_pillar_gb300 as P
+    w = W.generate(W.scaled("stress", B=18, length_scale=0.05, seed_offset=12))
+    g = Gpu(w, verify_chunk=128, draft_chunk=64)
+    g.attn()
+    assert g.attn_flags() == 0
+    unified = g.host()
+    g.out.zero_()
+    g.logits.zero_()
+    g.plan()
+    g.run()
+    first = g.host()
+    np.testing.assert_array_equal(first["out"], unified["out"])
+    np.testing.assert_array_equal(first["logits"], unified["logits"])
+    np.testing.assert_array_equal(first["lse"], unified["lse"])
+    k1 = g.k_pool
+    g.k_pool = k1 ^ torch.tensor(-32768, dtype=torch.int16, device="cuda")  # bf16 sign bit
+    g.out.zero_()
+    g.run()
+    assert g.attn_flags() == 0  # plan and both runs
+    w2 = copy.copy(w)
+    w2.k_logical = w.k_logical ^ np.uint16(0x8000)
+    compare_attn(w2, g.host(), run_oracle(w2))
+    g.k_pool = k1
+
+
 def test_repeated_calls_are_identical():
     w = W.generate(W.scaled("stress", B=15, length_scale=0.04, seed_offset=5))
     g = Gpu(w, verify_chunk=128)

@@ -64,6 +64,13 @@ class Gpu:
                               self.req_len, self.sparse_idx, self.sparse_cnt, self.out, self.logits, self.lse,
                               self.ws, stream=stream)
 
+    def plan(self, stream=None):
+        P.pillar_attn_plan(self.shape, self.req_mode, self.req_len, self.sparse_cnt, self.ws, stream=stream)
+
+    def run(self, stream=None):
+        P.pillar_attn_run(self.shape, self.q, self.k_pool, self.v_pool, self.slot_table, self.sparse_idx, self.out,
+                          self.logits, self.lse, self.ws, stream=stream)
+
     def topk(self, stream=None):
         P.pillar_topk_select(self.shape, self.V, self.logits, self.lse, self.req_len, self.group_map, self.K,
                              self.next_idx, self.next_cnt, self.tws, stream=stream)
