@@ -128,7 +128,10 @@ __global__ void __launch_bounds__(kScoreThreads) topk_scores_kernel(const TopkPa
     // kernels ahead on the stream are complete.
     pdl_launch_dependents();
     pdl_wait_prerequisites();
-    const int v = blockIdx.z, g = blockIdx.y;
+    // the verify requests in the reverse of the order in which the attention pass wrote their
+    // logits: the most recently written rows, the likeliest to be still in L2, are read first,
+    // before the pass's own reads push them out
+    const int v = (int)(gridDim.z - 1 - blockIdx.z), g = blockIdx.y;
     const int L = verify_len(p, v);
     const int t0 = blockIdx.x * kScoreChunk;
     const bool recorder = blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0;  // writes the request's record
