@@ -5,11 +5,13 @@
 // kernel.  A work item is (request, KV head, key range): verify requests are
 // split over their context into near-equal chunks of about verify_chunk keys,
 // draft lists into chunks of about draft_chunk listed keys.  Verify items are
-// listed first (they are the heavy ones), then draft items, so the work queue
-// is consumed roughly heaviest-first; a verify request's items are listed
-// chunk by chunk with the KV heads innermost, so the CTAs that read the same
-// positions (neighbouring 256-byte rows of the same slot blocks, one per
-// head) run at the same time.  The draft/verify mix in one batch is
+// listed first (they are the heavy ones), then draft items by size, largest
+// first, so the work queue is consumed heaviest-first and the last items
+// taken are the shortest (the longest-processing-time rule: the CTAs finish
+// close together); a verify request's items are listed chunk by chunk with
+// the KV heads innermost, so the CTAs that read the same positions
+// (neighbouring 256-byte rows of the same slot blocks, one per head) run at
+// the same time.  The draft/verify mix in one batch is
 // the unified batch of "SparseSpec-MLSys26" (Unified batch scheduler + fused
 // attention kernel); splitting long contexts over CTAs and merging the pieces
 // by their LSE is this implementation's own load balancing.
@@ -35,6 +37,22 @@ struct PlanParams {
 };
 
 constexpr int kScanN = 8;
+
+// Size bins of the draft items: bin i holds the items of the draft units whose
+// chunk spans kSizeBins - i tiles, so the bins in order are largest first.
+constexpr int kSizeBins = kMaxChunk / kTileKeys;
+
+// Size bin of a draft unit's items from its chunk size cs (an empty list
+// counts as one tile: its item still passes through the pipeline once).
+__device__ __forceinline__ int size_bin(int cs) {
+    const int tiles = cs > kTileKeys ? (cs + kTileKeys - 1) / kTileKeys : 1;
+    return kSizeBins - (tiles < kSizeBins ? tiles : kSizeBins);
+}
+
+// Units a planner thread keeps in registers between the scan and the item
+// emission (one per chunk of kPlanThreads units); beyond that many chunks
+// the emission re-reads its inputs.
+constexpr int kRegChunks = 2;
 
 // Exclusive scan of kScanN values per thread over the CTA (kPlanThreads
 // threads), all at once; tot[] gets the CTA totals.
@@ -141,11 +159,10 @@ __device__ __forceinline__ ReqInfo check_request(const PlanParams &p, int mode, 
 // they are listed chunk by chunk, head-minor (request, chunk, head), so the
 // Hkv items reading the same positions are taken up together.  Draft items
 // stay per unit.
-__device__ __forceinline__ void emit_items(const PlanParams &p, int u, const ReqInfo &r, int n, int ns, int cs,
-                                           int item_base) {
+__device__ __forceinline__ void emit_items(const PlanParams &p, int u, int mode, int n, int ns, int cs, int item_base) {
     const int g = u - (u / p.Hkv) * p.Hkv;
-    const int first = r.mode == 1 ? item_base - g * ns + g : item_base;
-    const int step = r.mode == 1 ? p.Hkv : 1;
+    const int first = mode == 1 ? item_base - g * ns + g : item_base;
+    const int step = mode == 1 ? p.Hkv : 1;
     for (int s = 0; s < ns; ++s) {
         Item it;
         it.unit = u;
@@ -158,7 +175,9 @@ __device__ __forceinline__ void emit_items(const PlanParams &p, int u, const Req
 
 // One thread per unit (request, KV head), chunks of kPlanThreads units; the
 // unit with g == 0 also carries its request's counts, so one fused scan per
-// chunk gives every offset.
+// chunk gives every offset.  A draft unit's items are placed in two steps:
+// its place inside its size bin while the chunks are scanned, the bin's
+// first index once every unit has been counted.
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     // the attention kernel may start its prologue (barriers, tensor memory) now;
     // it reads nothing of this kernel's output before this kernel completes
@@ -171,17 +190,21 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
         p.hdr->item_counter = 0;
     }
     int bad = 0;
-    // When one chunk covers every unit (U <= kPlanThreads), each thread keeps
-    // its unit's record and emits its items without reading anything back.
-    const bool one_chunk = U <= kPlanThreads;
-    ReqInfo r1;
-    int n1 = 0, ns1 = 1, cs1 = 0, item1 = 0;
+    // When at most kRegChunks chunks cover every unit, each thread keeps its
+    // units' records and emits their items without reading anything back.
+    const bool in_regs = U <= kRegChunks * kPlanThreads;
+    int modek[kRegChunks], nk[kRegChunks], nsk[kRegChunks], csk[kRegChunks], itemk[kRegChunks];
     // running totals of the chunks before (shared memory: no registers held across the scans):
     // q rows, kv positions, verify requests, logits, verify items, draft items, partial rows, merges
     __shared__ long long carry[kScanN];
+    __shared__ int s_bin[kSizeBins];  // draft items per size bin, then each bin's first item
+    // the naive joint batch walks each unit's items in place, so its drafts stay unit by unit
+    const bool by_size = p.schedule != PILLAR_SCHEDULE_NAIVE_JOINT;
     if (tid < kScanN) carry[tid] = 0;
+    if (tid < kSizeBins) s_bin[tid] = 0;
     __syncthreads();
-    for (int base = 0; base < U; base += kPlanThreads) {
+#pragma unroll 1
+    for (int base = 0, ci = 0; base < U; base += kPlanThreads, ++ci) {
         const int u = base + tid;
         const bool live = u < U;
         const int b = live ? u / p.Hkv : 0, g = live ? u - b * p.Hkv : 0;
@@ -220,16 +243,25 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
             ui.nsplit = ns;
             ui.rec_rows = rec_rows;
             ui.rec_base = (int)(carry[6] + v[6]);
-            // draft items follow every verify item: with one chunk the verify total is
-            // known here, otherwise the bases are relative and fixed up below
-            ui.item_base = (int)(r.mode == 1 ? carry[4] + v[4] : carry[5] + v[5] + (one_chunk ? tot[4] : 0));
+            // draft items follow every verify item; their bases are relative here (the place
+            // in the size bin, or among the drafts in unit order) and fixed up below
+            if (r.mode == 1)
+                ui.item_base = (int)(carry[4] + v[4]);
+            else if (by_size)
+                ui.item_base = ns > 0 ? atomicAdd(&s_bin[size_bin(cs)], ns) : 0;
+            else
+                ui.item_base = (int)(carry[5] + v[5]);
             p.unit[u] = ui;
-            if (one_chunk) {
-                r1 = r;
-                n1 = n;
-                ns1 = ns;
-                cs1 = cs;
-                item1 = ui.item_base;
+            if (in_regs) {
+#pragma unroll
+                for (int k = 0; k < kRegChunks; ++k)
+                    if (k == ci) {
+                        modek[k] = r.mode;
+                        nk[k] = n;
+                        nsk[k] = ns;
+                        csk[k] = cs;
+                        itemk[k] = ui.item_base;
+                    }
             }
             if (rec_rows > 0) {
                 // the request's first query row and verify index: the exclusive prefixes at
@@ -255,27 +287,50 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
         __syncthreads();
     }
     const long long ver_items = carry[4];
+    if (by_size && tid < 32) {  // each size bin's first item: after the verify items, largest bin first
+        static_assert(kSizeBins <= 32, "one warp lays out the bins");
+        const int own = tid < kSizeBins ? s_bin[tid] : 0;
+        int x = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (tid >= o) x += y;
+        }
+        if (tid < kSizeBins) s_bin[tid] = x - own + (int)ver_items;
+    }
+    __syncthreads();
     if (tid == 0) {
         p.hdr->num_items = (int)(carry[4] + carry[5]);
         p.hdr->num_units = U;
         p.hdr->num_merge = (int)carry[7];
     }
-    // Emit the items.
-    if (one_chunk) {
-        if (tid < U) emit_items(p, tid, r1, n1, ns1, cs1, item1);
+    // Emit the items, with the draft units' bases made absolute.
+    if (in_regs) {
+#pragma unroll
+        for (int k = 0; k < kRegChunks; ++k) {
+            const int u = k * kPlanThreads + tid;
+            if (u < U) {
+                int item = itemk[k];
+                if (modek[k] != 1) {
+                    item += by_size ? s_bin[size_bin(csk[k])] : (int)ver_items;
+                    p.unit[u].item_base = item;
+                }
+                emit_items(p, u, modek[k], nk[k], nsk[k], csk[k], item);
+            }
+        }
     } else {
         for (int u = tid; u < U; u += kPlanThreads) {  // each thread re-reads only the unit it wrote itself
             const int b = u / p.Hkv;
             int len, dummy = 0;
             const ReqInfo r = check_request(p, p.req_mode[b], p.req_len[b], &dummy, &len);
             UnitInfo ui = p.unit[u];
-            if (r.mode != 1) {
-                ui.item_base += (int)ver_items;
-                p.unit[u].item_base = ui.item_base;
-            }
             int n, ns;
             const int cs = unit_split(p, r, p.sparse_cnt[u], &n, &ns, &dummy);
-            emit_items(p, u, r, n, ns, cs, ui.item_base);
+            if (r.mode != 1) {
+                ui.item_base += by_size ? s_bin[size_bin(cs)] : (int)ver_items;
+                p.unit[u].item_base = ui.item_base;
+            }
+            emit_items(p, u, r.mode, n, ns, cs, ui.item_base);
         }
     }
     if (bad) atomicOr(&p.hdr->err, bad);

@@ -163,6 +163,23 @@ def test_naive_joint_batch_on_long_contexts():
     _check(w, n)
 
 
+@pytest.mark.parametrize("B", [120, 250, 300])
+def test_batches_over_several_planner_chunks(B):
+    """The planner takes its (request, KV head) units 1024 at a time: batches
+    of one, two and three such chunks (the third re-reads its inputs to emit
+    the items), with draft lists of many sizes and split units, under the
+    unified schedule (draft items queued by size) and the naive joint batch
+    (each unit's items in place); both match the oracle everywhere."""
+    import sparse_self_speculative_pillar_gb300 as P
+    w = W.generate(W.scaled("stress", B=B, length_scale=0.12, seed_offset=30 + B))
+    assert w.B * w.Hkv > (B // 128) * 1024
+    for kw in (dict(), dict(draft_chunk=128), dict(schedule=P.SCHEDULE_NAIVE_JOINT)):
+        g = Gpu(w, **kw)
+        g.attn()
+        assert g.attn_flags() == 0
+        _check(w, g)
+
+
 def test_one_plan_serves_several_runs():
     """pillar_attn_plan once, then pillar_attn_run for two layers of the same
     batch (the second with every key's sign flipped, exact in bf16): the first
