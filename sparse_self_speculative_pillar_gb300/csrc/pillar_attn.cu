@@ -75,7 +75,6 @@ struct AttnParams {
     const long long *kv_off, *logit_off;
     const UnitInfo *unit;
     const MergeUnit *merge_units;
-    int merge_cap;  // merge-unit slots in the workspace
     const Item *items;
     float *part_o, *part_lse;
     long long num_slots;
@@ -1075,25 +1074,38 @@ constexpr int kMergeCtasPerSm = 1;  // one large CTA per SM: the whole grid is r
 // Combines the partial rows of every split (request, KV head).  A split unit
 // has nrec records of nrows rows (M for verify, G for draft); the work is
 // flattened over (listed unit, row, four output dimensions), one thread each,
-// so that few, long units still spread over the whole GPU.  The planner's
-// MergeUnit record holds everything a task needs, so a thread issues its
-// record's load together with the unit count and then all its partials'
-// loads at once.  A thread merges its records in batches, carrying a running
+// so that few, long units still spread over the whole GPU: the verify units
+// (listed from the bottom of the merge list) with M rows each, then the
+// draft units (listed from the top) with their G rows.  The planner's
+// MergeUnit record holds everything a task needs, so a thread loads the unit
+// counts, its record, and then all its partials at once.  A thread merges its records in batches, carrying a running
 // max and sums between batches.
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kMergeThreads, kMergeCtasPerSm) merge_kernel(const AttnParams p) {
     pdl_wait_prerequisites();  // the partials come from the attention kernel
     // the attention kernel is complete: its work queue is reset for the next run on the same plan
     if (blockIdx.x == 0 && threadIdx.x == 0) p.hdr->item_counter = 0;
-    const int per_unit = p.M * (D / 4);  // thread slots per listed unit (rows up to M)
-    for (long long w = (long long)blockIdx.x * kMergeThreads + threadIdx.x; w < (long long)p.merge_cap * per_unit;
+    constexpr int C4 = D / 4;
+    const int vslot = p.M * C4, dslot = p.G * C4;  // thread slots of a verify unit, of a draft unit
+    const int nv = p.hdr->num_merge, nd = p.hdr->num_merge_draft, U = p.hdr->num_units;
+    const long long vtotal = (long long)nv * vslot, total = vtotal + (long long)nd * dslot;
+    for (long long w = (long long)blockIdx.x * kMergeThreads + threadIdx.x; w < total;
          w += (long long)gridDim.x * kMergeThreads) {
-        const int li = (int)(w / per_unit);
-        const int idx = (int)(w - (long long)li * per_unit);
-        const MergeUnit mu = p.merge_units[li];  // in flight with the count below (stale past it: unused)
-        if (li >= p.hdr->num_merge) break;      // li only grows along the loop
-        const int row = idx / (D / 4), c4 = idx - row * (D / 4);
-        if (row >= mu.nrows) continue;
+        int li, idx;
+        if (w < vtotal) {
+            li = (int)(w / vslot);
+            idx = (int)(w - (long long)li * vslot);
+        } else {
+            const long long w2 = w - vtotal;
+            const int k = (int)(w2 / dslot);
+            idx = (int)(w2 - (long long)k * dslot);
+            li = U - 1 - k;
+        }
+        const MergeUnit mu = p.merge_units[li];
+        const int row = idx / C4, c4 = idx - row * C4;
+        const float *pl = p.part_lse + (size_t)mu.rec_base + row;
+        const float4 *po = reinterpret_cast<const float4 *>(p.part_o + ((size_t)mu.rec_base + row) * D) + c4;
+        const size_t so = (size_t)mu.nrows * C4;
         float mx = neg_inf(), den = 0.f;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int r0 = 0; r0 < mu.nrec; r0 += kMergeBatch) {
@@ -1103,9 +1115,8 @@ __global__ void __launch_bounds__(kMergeThreads, 1) merge_kernel(const AttnParam
             for (int q = 0; q < kMergeBatch; ++q) {
                 const int r = r0 + q;
                 if (r < mu.nrec) {
-                    const size_t pr = (size_t)mu.rec_base + (size_t)r * mu.nrows + row;
-                    ls[q] = __ldcg(p.part_lse + pr);
-                    v[q] = __ldcg(reinterpret_cast<const float4 *>(p.part_o + pr * D) + c4);
+                    ls[q] = __ldcg(pl + (size_t)r * mu.nrows);
+                    v[q] = __ldcg(po + r * so);
                 } else {
                     ls[q] = neg_inf();
                     v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1241,7 +1252,6 @@ cudaError_t launch_attn(const AttnArgs &a, int nsm, cudaStream_t st) {
     p.logit_off = reinterpret_cast<const long long *>(a.ws + a.lay.logit_off);
     p.unit = reinterpret_cast<const UnitInfo *>(a.ws + a.lay.unit);
     p.merge_units = reinterpret_cast<const MergeUnit *>(a.ws + a.lay.merge_units);
-    p.merge_cap = (int)((a.lay.items - a.lay.merge_units) / sizeof(MergeUnit));
     p.items = reinterpret_cast<const Item *>(a.ws + a.lay.items);
     p.part_o = reinterpret_cast<float *>(a.ws + a.lay.part_o);
     p.part_lse = reinterpret_cast<float *>(a.ws + a.lay.part_lse);

@@ -67,8 +67,9 @@ struct WsHeader {
     int num_items;
     int item_counter;
     int num_units;
-    int num_merge;  // units whose partials the merge kernel combines
-    int pad[59];    // keeps the arrays 256-byte aligned
+    int num_merge;        // verify units whose partials the merge kernel combines (merge_units[0, num_merge))
+    int num_merge_draft;  // draft units it combines (merge_units[num_units - num_merge_draft, num_units))
+    int pad[58];          // keeps the arrays 256-byte aligned
 };
 
 // Byte offsets of the attention workspace sections.

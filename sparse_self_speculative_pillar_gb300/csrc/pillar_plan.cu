@@ -19,7 +19,9 @@
 // The planner also places the partial records: a (request, KV head) split
 // over several items writes one record per item, M = (k+1)*G rows for a
 // verify request, G rows for a draft token; the units that need combining
-// are listed for the merge kernel.
+// are listed for the merge kernel, the verify units from the start of the
+// list and the draft units from its end, so that the merge gives each unit
+// threads for its own rows only.
 #include "pillar_device.cuh"
 
 namespace pillar {
@@ -51,8 +53,9 @@ __device__ __forceinline__ int size_bin(int cs) {
 
 // Units a planner thread keeps in registers between the scan and the item
 // emission (one per chunk of kPlanThreads units); beyond that many chunks
-// the emission re-reads its inputs.
-constexpr int kRegChunks = 2;
+// the emission re-reads its inputs.  Two measured slower than one: the
+// registers they hold cost the whole kernel more than the re-reads.
+constexpr int kRegChunks = 1;
 
 // Exclusive scan of kScanN values per thread over the CTA (kPlanThreads
 // threads), all at once; tot[] gets the CTA totals.
@@ -198,10 +201,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     // q rows, kv positions, verify requests, logits, verify items, draft items, partial rows, merges
     __shared__ long long carry[kScanN];
     __shared__ int s_bin[kSizeBins];  // draft items per size bin, then each bin's first item
+    __shared__ int s_mdraft;          // split draft units: listed from the top of the merge list down
     // the naive joint batch walks each unit's items in place, so its drafts stay unit by unit
     const bool by_size = p.schedule != PILLAR_SCHEDULE_NAIVE_JOINT;
     if (tid < kScanN) carry[tid] = 0;
     if (tid < kSizeBins) s_bin[tid] = 0;
+    if (tid == 0) s_mdraft = 0;
     __syncthreads();
 #pragma unroll 1
     for (int base = 0, ci = 0; base < U; base += kPlanThreads, ++ci) {
@@ -227,10 +232,26 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
             }
             if (r.mode == 1) v[4] = ns; else v[5] = ns;
             v[6] = (long long)ns * rec_rows;
-            v[7] = rec_rows > 0;
+            v[7] = rec_rows > 0 && r.mode == 1;
         }
         long long tot[kScanN];
         block_scan8(v, tot);
+        // A draft unit's place in its size bin.  The units of a warp with the same bin and split
+        // count take consecutive places through one shared atomic (the whole warp is here,
+        // converged after the scan), so the bin counters see a few atomics per warp and the
+        // items of neighbouring units are written next to each other.
+        int bin_place = 0;
+        if (by_size) {
+            const bool placed = live && r.mode != 1 && ns > 0;
+            const int bin = placed ? size_bin(cs) : -1;
+            const unsigned peers = __match_any_sync(0xffffffffu, bin) & __match_any_sync(0xffffffffu, placed ? ns : -1);
+            if (placed) {
+                const int lane = tid & 31, leader = __ffs(peers) - 1;
+                int first = 0;
+                if (lane == leader) first = atomicAdd(&s_bin[bin], __popc(peers) * ns);
+                bin_place = __shfl_sync(peers, first, leader) + __popc(peers & ((1u << lane) - 1)) * ns;
+            }
+        }
         if (live) {
             if (g == 0) {
                 r.q_off = (int)(carry[0] + v[0]);
@@ -248,7 +269,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
             if (r.mode == 1)
                 ui.item_base = (int)(carry[4] + v[4]);
             else if (by_size)
-                ui.item_base = ns > 0 ? atomicAdd(&s_bin[size_bin(cs)], ns) : 0;
+                ui.item_base = bin_place;
             else
                 ui.item_base = (int)(carry[5] + v[5]);
             p.unit[u] = ui;
@@ -276,7 +297,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
                 mu.verify = r.mode == 1;
                 mu.orow0 = q_off * p.Hq + (long long)g * G;
                 mu.lse0 = r.mode == 1 ? (vidx * p.Hq + (long long)g * G) * (p.k + 1) : -1;
-                p.merge_units[carry[7] + v[7]] = mu;
+                p.merge_units[r.mode == 1 ? carry[7] + v[7] : U - 1 - atomicAdd(&s_mdraft, 1)] = mu;
             }
         }
         __syncthreads();  // every thread has read this chunk's carries
@@ -303,6 +324,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
         p.hdr->num_items = (int)(carry[4] + carry[5]);
         p.hdr->num_units = U;
         p.hdr->num_merge = (int)carry[7];
+        p.hdr->num_merge_draft = s_mdraft;
     }
     // Emit the items, with the draft units' bases made absolute.
     if (in_regs) {
