@@ -182,6 +182,10 @@ __device__ __forceinline__ void emit_items(const PlanParams &p, int u, int mode,
 // its place inside its size bin while the chunks are scanned, the bin's
 // first index once every unit has been counted.
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
+    // launched as a programmatic dependent of the kernel before it on the stream (the last
+    // step's Top-K, or another layer's run on this workspace): nothing is read or written
+    // before the kernels ahead are complete
+    pdl_wait_prerequisites();
     // the attention kernel may start its prologue (barriers, tensor memory) now;
     // it reads nothing of this kernel's output before this kernel completes
     pdl_launch_dependents();
@@ -379,8 +383,18 @@ cudaError_t launch_plan(const PlanArgs &a, cudaStream_t st) {
     p.vchunk = a.vchunk;
     p.dchunk = a.dchunk;
     p.schedule = a.schedule;
-    plan_kernel<<<1, kPlanThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    // a programmatic dependent of the kernel before it: its launch overlaps that kernel's tail
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, plan_kernel, p);
 }
 
 }  // namespace pillar

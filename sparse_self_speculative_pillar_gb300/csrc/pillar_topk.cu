@@ -350,6 +350,7 @@ __global__ void __launch_bounds__(kSelectThreads, 1) topk_select_kernel(const To
     uint32_t *cand = fine_b + kFineBins;
     uint32_t(*whist)[256] = reinterpret_cast<uint32_t(*)[256]>(cand + kCandCap);
     __shared__ uint32_t s_bin, s_rank, s_ncand, s_wsum[kSelectWarps];
+    pdl_launch_dependents();   // the next kernel (the next step's planner) may be scheduled now
     pdl_wait_prerequisites();  // the scores and the score pass's records are complete and visible
     const int v = blockIdx.y, g = blockIdx.x, tid = threadIdx.x;
     const TopkRow rec = p.rows[v];
