@@ -30,6 +30,11 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
 // memory is visible (a no-op when it was launched without the attribute).
 __device__ __forceinline__ void pdl_wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Brings the 128-byte line of addr into L2 (a hint: no data is returned, nothing is ordered).
+__device__ __forceinline__ void l2_prefetch(const void *addr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {

@@ -184,7 +184,17 @@ __device__ __forceinline__ void emit_items(const PlanParams &p, int u, int mode,
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     // launched as a programmatic dependent of the kernel before it on the stream (the last
     // step's Top-K, or another layer's run on this workspace): nothing is read or written
-    // before the kernels ahead are complete
+    // before the kernels ahead are complete.  The inputs' lines are only prefetched into L2
+    // meanwhile (a hint: the loads below read them after the wait, through the coherent L2).
+    {
+        const int U0 = p.B * p.Hkv;
+        const int t = threadIdx.x;
+        for (int l = t; l * 32 < U0; l += kPlanThreads) l2_prefetch(p.sparse_cnt + l * 32);
+        if (t * 32 < p.B) {
+            l2_prefetch(p.req_mode + t * 32);
+            l2_prefetch(p.req_len + t * 32);
+        }
+    }
     pdl_wait_prerequisites();
     // the attention kernel may start its prologue (barriers, tensor memory) now;
     // it reads nothing of this kernel's output before this kernel completes
