@@ -83,7 +83,7 @@ typedef struct pillar_shape {
     int32_t max_topk;      /* row stride of next_idx (>= 1) */
     int32_t verify_chunk;  /* keys per verify work item (multiple of 64, <= 2048); 0: 1024 for
                               contexts under 8192 positions, 2048 from 8192 on */
-    int32_t draft_chunk;   /* listed keys per draft work item (multiple of 64, <= 2048; 0 = 1024) */
+    int32_t draft_chunk;   /* listed keys per draft work item (multiple of 64, <= 2048; 0 = 2048) */
     int64_t num_slots;     /* rows of k_pool / v_pool */
     float sm_scale;        /* logit scale; 0 means 1/sqrt(D) */
     int32_t schedule;      /* PILLAR_SCHEDULE_* (0: the unified pass) */

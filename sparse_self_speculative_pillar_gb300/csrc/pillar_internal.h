@@ -24,7 +24,7 @@ constexpr int kMaxG = 8;               // query heads per KV head
 constexpr int kDefaultVerifyChunk = 1024;
 constexpr int kLongVerifyChunk = 2048;
 constexpr int kLongContext = 8192;
-constexpr int kDefaultDraftChunk = 1024;
+constexpr int kDefaultDraftChunk = 2048;
 constexpr int kMaxChunk = 2048;        // item key bound (sizes the resolved row lists in shared memory)
 constexpr int kPlanThreads = 1024;
 constexpr unsigned long long kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s: the default wait bound, and the drains'

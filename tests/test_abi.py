@@ -108,7 +108,7 @@ def test_workspace_covers_the_most_items_the_planner_can_emit():
     """The planner splits a verify request of L keys into ceil(L / chunk)
     items (chunk = verify_chunk, or by default 1024 keys below 8192 positions
     and 2048 from there on) and a draft list of n keys into ceil(n /
-    draft_chunk) items; every item of a split (request, KV head) writes
+    draft_chunk) items (2048 keys by default); every item of a split (request, KV head) writes
     (k+1)*G partial rows of D fp32 values plus an LSE.  The workspace must
     hold that many item records and partial rows for the worst batch of the
     shape."""
@@ -125,7 +125,7 @@ def test_workspace_covers_the_most_items_the_planner_can_emit():
                    verify_chunk=vc, draft_chunk=dc, row_lo=min(1, k), row_hi=k + 1)
         units = s.B * Hkv
         v_items = -(-s.max_len // (vc or 1024))          # the default's smaller chunk gives the most items
-        d_items = -(-s.max_sparse // (dc or 1024)) if s.max_sparse else 1
+        d_items = -(-s.max_sparse // (dc or 2048)) if s.max_sparse else 1  # draft items: 2048 keys by default
         items = units * max(v_items, d_items, 1)
         rows = items * (k + 1) * G
         need = items * 16 + rows * (D + 1) * 4              # item records + partial rows (D values + LSE)
