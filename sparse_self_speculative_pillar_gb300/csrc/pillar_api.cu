@@ -266,7 +266,7 @@ int pillar_topk_select(const pillar_shape_t *shape, int32_t V, const float *veri
     ta.row_hi = shape->row_hi;
     ta.max_topk = shape->max_topk;
     ta.max_len = shape->max_len;
-    if (cudaMemsetAsync(ta.ws, 0, sizeof(int), cs) != cudaSuccess) return PILLAR_ERR_CUDA;
+    // (the score kernel clears the error word itself: no memset between the attention and the Top-K)
     if (launch_topk_select(ta, cs) != cudaSuccess) return PILLAR_ERR_CUDA;
     return PILLAR_OK;
 }

@@ -128,6 +128,10 @@ __global__ void __launch_bounds__(kScoreThreads) topk_scores_kernel(const TopkPa
     // kernels ahead on the stream are complete.
     pdl_launch_dependents();
     pdl_wait_prerequisites();
+    // The workspace's error word starts the call at zero: no block of this grid writes it, and
+    // the select (the only kernel of the call that flags) runs once this grid has completed.
+    // No memset has to come between the attention's kernels and this one.
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) p.hdr->err = 0;
     // the verify requests in the reverse of the order in which the attention pass wrote their
     // logits: the most recently written rows, the likeliest to be still in L2, are read first,
     // before the pass's own reads push them out
@@ -135,8 +139,7 @@ __global__ void __launch_bounds__(kScoreThreads) topk_scores_kernel(const TopkPa
     const int L = verify_len(p, v);
     const int t0 = blockIdx.x * kScoreChunk;
     const bool recorder = blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0;  // writes the request's record
-    if (L < 0 || L > p.max_len) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&p.hdr->err, PILLAR_FLAG_REQUEST);
+    if (L < 0 || L > p.max_len) {  // skipped; the select flags it from the record
         if (recorder) p.rows[v] = TopkRow{-1, 0, 0};
         return;
     }
@@ -355,8 +358,11 @@ __global__ void __launch_bounds__(kSelectThreads, 1) topk_select_kernel(const To
     const int v = blockIdx.y, g = blockIdx.x, tid = threadIdx.x;
     const TopkRow rec = p.rows[v];
     const int L = rec.L;
-    if (L < 0 || L > p.max_len) {
-        if (tid == 0) p.next_cnt[v * p.Hkv + g] = 0;
+    if (L < 0 || L > p.max_len) {  // a request the score pass skipped (group_map entry or length)
+        if (tid == 0) {
+            p.next_cnt[v * p.Hkv + g] = 0;
+            if (g == 0) atomicOr(&p.hdr->err, PILLAR_FLAG_REQUEST);
+        }
         return;
     }
     int K = rec.K;

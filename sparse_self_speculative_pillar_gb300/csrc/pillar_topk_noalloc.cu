@@ -78,8 +78,9 @@ int pillar_topk_select_noalloc(const pillar_shape_t *shape, int32_t V, const flo
     char *ws = static_cast<char *>(scratch_for_current_device());
     if (!ws) return PILLAR_ERR_CUDA;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    // the array keeps the previous call's contents: the error word must start at zero
-    if (cudaMemsetAsync(ws, 0, sizeof(int), cs) != cudaSuccess) return PILLAR_ERR_CUDA;
+    // the array keeps the previous call's contents: the error word must start at zero (the score
+    // kernel clears it when there is a verify request)
+    if (V == 0 && cudaMemsetAsync(ws, 0, sizeof(int), cs) != cudaSuccess) return PILLAR_ERR_CUDA;
     if (V > 0) {
         TopkArgs ta;
         ta.logits = verify_logits;
