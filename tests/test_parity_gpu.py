@@ -406,6 +406,32 @@ def test_topk_skips_bad_group_map_and_negative_lengths():
     compare_topk(ni[:1], nc[:1], ref, [L], [K], Hkv)
 
 
+def test_topk_error_word_reports_each_call_alone():
+    """Every Top-K call starts from a clean error word (its score kernel
+    clears it): a flagged call followed by a clean one, with no read in
+    between, reports nothing, and a clean call followed by a flagged one
+    reports the flag (the entry point without a workspace: test_zz_no_alloc)."""
+    import sparse_self_speculative_pillar_gb300 as P
+    Hq, Hkv, k, L, K = 4, 2, 2, 200, 9
+    rng = np.random.default_rng(43)
+    lg = rng.standard_normal((1, Hq, k + 1, L)).astype(np.float32)
+    lse = np.log(np.exp(lg.astype(np.float64)).sum(-1)).astype(np.float32)
+    shape = P.make_shape(B=2, Hq=Hq, Hkv=Hkv, D=64, k=k, max_sparse=1, max_len=L, num_slots=1, max_topk=K)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    args = [dev(lg.ravel()), dev(lse), dev(np.array([L, 50], np.int32))]
+    good, bad = dev(np.array([0], np.int32)), dev(np.array([7], np.int32))  # batch index 7: no such request
+    Kd = dev(np.array([K], np.int32))
+    nidx = torch.full((1, Hkv, K), -1, dtype=torch.int32, device="cuda")
+    ncnt = torch.full((1, Hkv), -1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(P.pillar_topk_workspace_bytes(shape, 1), dtype=torch.uint8, device="cuda")
+    P.pillar_topk_select(shape, 1, *args, bad, Kd, nidx, ncnt, ws)
+    P.pillar_topk_select(shape, 1, *args, good, Kd, nidx, ncnt, ws)
+    assert P.pillar_get_error(ws) == 0
+    P.pillar_topk_select(shape, 1, *args, good, Kd, nidx, ncnt, ws)
+    P.pillar_topk_select(shape, 1, *args, bad, Kd, nidx, ncnt, ws)
+    assert P.pillar_get_error(ws) == P.FLAG_REQUEST
+
+
 def test_verify_shorter_than_its_rows_gives_finite_topk():
     """A verify request with L < k+1 is flagged but computed: its first rows
     see no position (LSE -inf, every logit -inf).  Averaging those rows too,

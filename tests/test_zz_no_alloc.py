@@ -55,3 +55,26 @@ def test_noalloc_topk_refuses_shapes_beyond_its_scratch():
     # the largest shape that fits is accepted
     shape_ok = P.make_shape(B=8, Hq=32, Hkv=8, D=128, k=8, max_sparse=1, max_len=65535, num_slots=1, max_topk=16)
     assert P.pillar_topk_workspace_bytes(shape_ok, 8) <= P.NOALLOC_SCRATCH_BYTES
+
+
+def test_noalloc_error_word_reports_each_call_alone():
+    """The built-in scratch keeps the previous call's contents; its error word
+    starts every call clean all the same: a flagged call followed by a clean
+    one reports nothing, a clean one followed by a flagged one the flag."""
+    Hq, Hkv, k, L, K = 4, 2, 2, 200, 9
+    rng = np.random.default_rng(44)
+    lg = rng.standard_normal((1, Hq, k + 1, L)).astype(np.float32)
+    lse = np.log(np.exp(lg.astype(np.float64)).sum(-1)).astype(np.float32)
+    shape = P.make_shape(B=2, Hq=Hq, Hkv=Hkv, D=64, k=k, max_sparse=1, max_len=L, num_slots=1, max_topk=K)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    args = [dev(lg.ravel()), dev(lse), dev(np.array([L, 50], np.int32))]
+    good, bad = dev(np.array([0], np.int32)), dev(np.array([7], np.int32))  # batch index 7: no such request
+    Kd = dev(np.array([K], np.int32))
+    nidx = torch.full((1, Hkv, K), -1, dtype=torch.int32, device="cuda")
+    ncnt = torch.full((1, Hkv), -1, dtype=torch.int32, device="cuda")
+    flags = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    P.pillar_topk_select_noalloc(shape, 1, *args, bad, Kd, nidx, ncnt, device_flags=flags)
+    P.pillar_topk_select_noalloc(shape, 1, *args, good, Kd, nidx, ncnt, device_flags=flags)
+    assert int(flags.item()) == 0
+    P.pillar_topk_select_noalloc(shape, 1, *args, bad, Kd, nidx, ncnt, device_flags=flags)
+    assert int(flags.item()) == P.FLAG_REQUEST
