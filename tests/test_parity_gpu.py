@@ -320,6 +320,31 @@ def test_edge_lengths_and_lists():
     assert np.all(res["out"][w.q_off[1], 4:8] == 0)    # empty list of KV head 1
 
 
+def test_growing_row_maxima_rescale_the_output():
+    """Keys scaled up along the context (position t by 1 + t/128), so that a
+    row's maximum score keeps rising from tile to tile by more than the kernel's
+    2^8 rescale threshold: the path that rescales the accumulated output rows,
+    which the workloads' N(0, 1) scores never reach, against the oracle."""
+    w = W.generate(W.scaled("qwen3_8b", B=12, length_scale=0.3, seed_offset=41))
+    K = W.bf16_bits_to_f32(w.k_logical.view(np.uint16)).astype(np.float32)
+    for b in range(w.B):
+        lo, L = int(w.kv_off[b]), int(w.req_len[b])
+        K[lo:lo + L] *= (1.0 + np.arange(L, dtype=np.float32) / 128.0)[:, None, None]
+    w.k_logical = W.f32_to_bf16_bits(K)
+    # the inputs do what the test is for: in the first verify request's last row (head 0), a
+    # 64-key tile of the first 1024 keys beats the maximum of the tiles before it by > 8 ln 2
+    b = int(np.nonzero(w.req_mode == 1)[0][0])
+    lo, L = int(w.kv_off[b]), int(w.req_len[b])
+    q = W.bf16_bits_to_f32(w.q[int(w.q_off[b]) + w.k, 0].view(np.uint16)).astype(np.float64)
+    s = (W.bf16_bits_to_f32(w.k_logical[lo:lo + min(L, 1024), 0].view(np.uint16)) @ q) / math.sqrt(w.D)
+    tiles = [s[i:i + 64].max() for i in range(0, len(s), 64)]
+    assert max(tiles[i] - max(tiles[:i]) for i in range(1, len(tiles))) > 8 * math.log(2)
+    g = Gpu(w)
+    g.attn()
+    assert g.attn_flags() == 0
+    _check(w, g)
+
+
 def test_out_of_range_entries_are_flagged_and_skipped():
     w = W.generate(W.scaled("qwen3_8b", B=4, length_scale=0.02, seed_offset=20))
     b = int(np.nonzero(w.req_mode == 0)[0][0])
