@@ -167,7 +167,7 @@ struct Ctx {
     uint64_t *o_done;                // [2]: an item's last P V has completed (per O buffer)
     uint64_t *epi_full, *epi_empty;  // [kEpiWarps * 2]: mailbox slots
     EpiRec *epi;                     // [kEpiWarps * 2]
-    float2 *epi_inv;                 // [kEpiWarps * 2][32]: 1/l of each thread's two rows
+    float2 *epi_l;                   // [kEpiWarps * 2][32]: the softmax sums l of each thread's two rows
     int4 *pend;  // [kSBuf] tiles between their S and P V MMAs (MMA thread only)
     volatile int *abort;
     uint32_t *tmem_slot;
@@ -199,7 +199,7 @@ __device__ __forceinline__ Ctx make_ctx(char *smem, const AttnParams &p) {
     c.epi_full = c.o_done + 2;
     c.epi_empty = c.epi_full + 2 * kEpiWarps;
     c.epi = reinterpret_cast<EpiRec *>(smem + S::off_epi);
-    c.epi_inv = reinterpret_cast<float2 *>(smem + S::off_epi + 2 * kEpiWarps * 32);
+    c.epi_l = reinterpret_cast<float2 *>(smem + S::off_epi + 2 * kEpiWarps * 32);
     c.pend = reinterpret_cast<int4 *>(smem + S::off_pend);
     c.abort = reinterpret_cast<volatile int *>(smem + S::off_misc);
     c.tmem_slot = reinterpret_cast<uint32_t *>(smem + S::off_misc + 4);
@@ -629,14 +629,28 @@ struct CState {
     uint32_t items;   // items handed to the epilogue warp (their mailbox slot alternates)
 };
 
+// The softmax warps' code is kept small: their loop slows with every instruction it holds, taken
+// or not (instruction-fetch stalls; measured on the Qwen3-8B-shaped step, where the rare paths
+// below moved out of line, the visibility test made one 64-bit mask applied after one multiply
+// path and the division moved to the epilogue warps took the step from 202.7 to 197.2 us).
+// Hence mbar_wait for these warps: the first test inline, the bounded polling out of line.
+__device__ __noinline__ bool mbar_wait_poll(uint64_t *bar, uint32_t parity, volatile int *abort, int *err,
+                                            unsigned long long limit_ns) {
+    return mbar_wait(bar, parity, abort, err, limit_ns);
+}
+__device__ __forceinline__ bool mbar_wait_c(uint64_t *bar, uint32_t parity, volatile int *abort, int *err,
+                                            unsigned long long limit_ns) {
+    return mbar_try_wait(bar, parity) || mbar_wait_poll(bar, parity, abort, err, limit_ns);
+}
+
 // Hands the next mailbox slot of this warp's quadrant to its epilogue warp
 // (waiting, bounded, for the slot to have been taken two records back).
-__device__ __forceinline__ bool post_epilogue(const Ctx &c, int warp, int lane, CState &cs, const EpiRec &e, float2 inv) {
+__device__ __forceinline__ bool post_epilogue(const Ctx &c, int warp, int lane, CState &cs, const EpiRec &e, float2 l) {
     const int slot = warp * 2 + (int)(cs.items & 1);
     const uint32_t use = cs.items >> 1;  // earlier uses of this slot
-    if (!mbar_wait(&c.epi_empty[slot], (use & 1) ^ 1, c.abort, c.err, c.wait_ns)) return false;
+    if (!mbar_wait_c(&c.epi_empty[slot], (use & 1) ^ 1, c.abort, c.err, c.wait_ns)) return false;
     if (lane == 0) c.epi[slot] = e;
-    c.epi_inv[slot * 32 + lane] = inv;
+    c.epi_l[slot * 32 + lane] = l;
     __syncwarp();
     if (lane == 0) mbar_arrive(&c.epi_full[slot]);
     ++cs.items;
@@ -683,24 +697,24 @@ template <int OFF>
 __device__ __forceinline__ float row_scores(const AttnParams &p, const StageMeta &cur, const VRow &r, float *s, int cq,
                                             bool verify) {
     if (!r.act) return neg_inf();
-    const bool interior = cur.nk == kTileKeys && cur.valid == ~0ull && cur.pos0 + kTileKeys - 1 <= r.lim;
-    if (interior) {
-        const float2 sc = make_float2(p.scale, p.scale);
+    // the row's visible keys of the tile: listed with a valid slot (the valid mask has no bit at or
+    // past nk) and, for a verify row, at or before its causal limit
+    const int span = r.lim - cur.pos0;
+    const unsigned long long vis = cur.valid & (span >= 63 ? ~0ull : span < 0 ? 0ull : (2ull << span) - 1);
+    const float2 sc = make_float2(p.scale, p.scale);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {  // packed pairs: one fp32x2 multiply per two scores
-            const float2 v = fmul2(make_float2(s[4 * c + OFF], s[4 * c + OFF + 1]), sc);
-            s[4 * c + OFF] = v.x;
-            s[4 * c + OFF + 1] = v.y;
-        }
-    } else {
+    for (int c = 0; c < 8; ++c) {  // packed pairs: one fp32x2 multiply per two scores
+        const float2 v = fmul2(make_float2(s[4 * c + OFF], s[4 * c + OFF + 1]), sc);
+        s[4 * c + OFF] = v.x;
+        s[4 * c + OFF + 1] = v.y;
+    }
+    if (vis != ~0ull) {  // keys this row does not see
+        const unsigned long long m = vis >> cq;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int key = 8 * c + cq + e;
-                const bool vis = key < cur.nk && ((cur.valid >> key) & 1ull) && cur.pos0 + key <= r.lim;
-                s[4 * c + OFF + e] = vis ? s[4 * c + OFF + e] * p.scale : neg_inf();
-            }
+            for (int e = 0; e < 2; ++e)
+                if (!((m >> (8 * c + e)) & 1ull)) s[4 * c + OFF + e] = neg_inf();
     }
     // maximum as a tree (short dependency chains)
     float m8[8];
@@ -714,24 +728,17 @@ __device__ __forceinline__ float row_scores(const AttnParams &p, const StageMeta
     if (!verify) return mt;
     // the row's four threads write 8 consecutive positions per chunk
     float *dst = p.logits + r.lb + cur.pos0 + cq;
-    if (cur.nk == kTileKeys) {
-        if (((r.lb + cur.pos0) & 1) == 0) {
+    if (cur.nk == kTileKeys && ((r.lb + cur.pos0) & 1) == 0) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<float2 *>(dst + 8 * c) = make_float2(s[4 * c + OFF], s[4 * c + OFF + 1]);
-        } else {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                dst[8 * c] = s[4 * c + OFF];
-                dst[8 * c + 1] = s[4 * c + OFF + 1];
-            }
-        }
-    } else {
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float2 *>(dst + 8 * c) = make_float2(s[4 * c + OFF], s[4 * c + OFF + 1]);
+    } else {  // a row that starts on an odd float, or the keys of a partial tile: one float at a time
+        const int lim = cur.nk - cq;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
 #pragma unroll
             for (int e = 0; e < 2; ++e)
-                if (8 * c + cq + e < cur.nk) dst[8 * c + e] = s[4 * c + OFF + e];
+                if (8 * c + e < lim) dst[8 * c + e] = s[4 * c + OFF + e];
     }
     return mt;
 }
@@ -777,8 +784,7 @@ __device__ __forceinline__ void row_output(const AttnParams &p, const ItemInfo &
 }
 
 // Scales this thread's two O rows by aa (row A) and ab (row B) after a running maximum grew by
-// more than 2^8.  Out of line: the call is rare, and the softmax loop slows with every
-// instruction it holds, taken or not (measured: -0.7 us on the Qwen3-8B-shaped step).
+// more than 2^8 (rare; out of line).
 template <int D>
 __device__ __noinline__ bool rescale_o(uint64_t *sfree, uint32_t par, volatile int *abort, int *err,
                                        unsigned long long wait_ns, uint32_t taddr, float aa, float ab) {
@@ -800,6 +806,9 @@ __device__ __noinline__ bool rescale_o(uint64_t *sfree, uint32_t par, volatile i
     }
     return true;
 }
+
+// A row's LSE from its running maximum and sum (once per item; out of line).
+__device__ __noinline__ void put_lse(float *dst, float m, float l) { *dst = l > 0.f ? m + logf(l) : neg_inf(); }
 
 // The consumer side of an item.  The warp reads lanes 0-15 of
 // its TMEM quadrant with the 16x256b shape: each row (lane) is shared by four
@@ -823,7 +832,7 @@ __device__ bool attn_item(const AttnParams &p, const Ctx &c, int warp, int lane,
         const uint32_t vt = cs.vt, sb = vt % kSBuf;
         __syncwarp();
         if (lane == 0) mbar_arrive(&c.empty[cs.stage]);  // the stage is read by the tensor cores only
-        if (!mbar_wait(&c.s_full[sb], (vt / kSBuf) & 1, c.abort, c.err, c.wait_ns)) return false;
+        if (!mbar_wait_c(&c.s_full[sb], (vt / kSBuf) & 1, c.abort, c.err, c.wait_ns)) return false;
         tc_fence_after();
         const uint32_t tS = cs.tbase + sb * kTileKeys;
         float s[32];
@@ -879,7 +888,7 @@ __device__ bool attn_item(const AttnParams &p, const Ctx &c, int warp, int lane,
             cs.phase ^= 1;
         }
         if (last) break;
-        if (!mbar_wait(&c.full[cs.stage], cs.phase, c.abort, c.err, c.wait_ns)) return false;
+        if (!mbar_wait_c(&c.full[cs.stage], cs.phase, c.abort, c.err, c.wait_ns)) return false;
         cur = c.meta[cs.stage];
     }
 
@@ -888,18 +897,15 @@ __device__ bool attn_item(const AttnParams &p, const Ctx &c, int warp, int lane,
     ra.l += __shfl_xor_sync(0xffffffffu, ra.l, 2);
     rb.l += __shfl_xor_sync(0xffffffffu, rb.l, 1);
     rb.l += __shfl_xor_sync(0xffffffffu, rb.l, 2);
-    const float inva = ra.l > 0.f ? 1.f / ra.l : 0.f, invb = rb.l > 0.f ? 1.f / rb.l : 0.f;
     if ((lane & 3) == 0 && (verify || in.nsplit > 1)) {
         const int kk1 = p.k + 1;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const VRow &r = h ? rb : ra;
             if (!r.act) continue;
-            const float lse = r.l > 0.f ? r.m + logf(r.l) : neg_inf();
-            if (in.nsplit == 1)
-                p.lse[((size_t)in.vidx * p.Hq + (size_t)in.g * p.G + r.gi) * kk1 + r.j] = lse;
-            else
-                p.part_lse[(size_t)in.rec + r.row] = lse;
+            put_lse(in.nsplit == 1 ? p.lse + ((size_t)in.vidx * p.Hq + (size_t)in.g * p.G + r.gi) * kk1 + r.j
+                                   : p.part_lse + (size_t)in.rec + r.row,
+                    r.m, r.l);
         }
     }
     // the O rows are written by the epilogue warp of this quadrant once the item's last P V has
@@ -914,7 +920,7 @@ __device__ bool attn_item(const AttnParams &p, const Ctx &c, int warp, int lane,
     e.qb = qb;
     e.stop = 0;
     e.pad = 0;
-    return post_epilogue(c, warp, lane, cs, e, make_float2(inva, invb));
+    return post_epilogue(c, warp, lane, cs, e, make_float2(ra.l, rb.l));
 }
 
 // The epilogue warp of quadrant q: for each item of the consumer warp of its
@@ -931,7 +937,8 @@ __device__ void epilogue_warp(const AttnParams &p, const Ctx &c, int q, int lane
         const int slot = q * 2 + (int)(n & 1);
         if (!mbar_wait(&c.epi_full[slot], (n >> 1) & 1, c.abort, c.err, c.wait_ns)) break;
         const EpiRec e = c.epi[slot];
-        const float2 inv = c.epi_inv[slot * 32 + lane];
+        const float2 l = c.epi_l[slot * 32 + lane];  // (the division is done here, off the softmax warps' code)
+        const float2 inv = make_float2(l.x > 0.f ? 1.f / l.x : 0.f, l.y > 0.f ? 1.f / l.y : 0.f);
         __syncwarp();
         if (lane == 0) mbar_arrive(&c.epi_empty[slot]);  // the record is copied: the slot may be reused
         if (e.stop) break;
@@ -951,7 +958,7 @@ __device__ void epilogue_warp(const AttnParams &p, const Ctx &c, int q, int lane
         const VRow rb = item_row(p, in, verify, q, 8 + (lane >> 2));
         const bool have_b = (verify ? p.RQ : p.RQd) > 8;
         const uint32_t tO = tbase + S::tO + (uint32_t)e.qb * D;
-#pragma unroll
+#pragma unroll 1  // (rolled: less code beside the softmax warps' on each sub-partition)
         for (int c0 = 0; c0 < D; c0 += 64) {
             float ov[32];
             tmem_ld16x256b_x8(tO + lane_base + c0, ov);  // warp-collective: every lane loads
@@ -976,7 +983,7 @@ __device__ void consumer(const AttnParams &p, const Ctx &c, int warp, int lane, 
     cs.tbase = tbase;
     cs.items = 0;
     for (;;) {
-        if (!mbar_wait(&c.full[cs.stage], cs.phase, c.abort, c.err, c.wait_ns)) break;
+        if (!mbar_wait_c(&c.full[cs.stage], cs.phase, c.abort, c.err, c.wait_ns)) break;
         const StageMeta m = c.meta[cs.stage];
         if (m.flags & kStop) break;
         if (!attn_item<D>(p, c, warp, lane, cs, m)) break;
