@@ -695,8 +695,10 @@ __device__ __forceinline__ VRow item_row(const AttnParams &p, const ItemInfo &in
     r.l = 0.f;
     if (r.act && verify) {
         const int kk1 = p.k + 1;
-        r.j = r.row / p.G;
-        r.gi = r.row - r.j * p.G;
+        int j = 0, gi = r.row;  // row / G by subtraction (at most k+1 steps; less code than a division)
+        while (gi >= p.G) gi -= p.G, ++j;
+        r.j = j;
+        r.gi = gi;
         r.lim = in.L - kk1 + r.j;
         r.lb = in.logit_off + ((long long)(in.g * p.G + r.gi) * kk1 + r.j) * in.L;
     }
